@@ -1,0 +1,237 @@
+"""Pins for the CPU oracle: closed forms, invariants and exact brute force.
+
+Each case is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign, a swapped index, a transposed operand, a wrong layout offset, beta
+applied when it should not be) fails at least one of them. None of these tests
+retypes the oracle's own formula: they compare it with facts that hold by
+construction (identity, permutation, all-ones, rank one), with exact rational
+arithmetic, or with an independent library routine.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_gemm_cluster_gb300 import inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def bf16(rows, cols, seed, dist="normal", scale=1.0):
+    return inputs.bf16_matrix(rows, cols, dist, seed, scale)
+
+
+def val(bits):
+    return inputs.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def eye_bf16(n):
+    return inputs.f64_to_bf16_bits(np.eye(n))
+
+
+def perm_bf16(perm):
+    n = len(perm)
+    P = np.zeros((n, n))
+    P[np.arange(n), perm] = 1.0          # row i of P selects column perm[i]
+    return inputs.f64_to_bf16_bits(P)
+
+
+def run(A_log, B_log, la="row", lb="row", alpha=1.0, beta=0.0, C_log=None, lc="row"):
+    M, K = A_log.shape
+    N = B_log.shape[1]
+    A, lda = inputs.store(A_log, la)
+    B, ldb = inputs.store(B_log, lb)
+    if C_log is not None:
+        C, ldc = inputs.store(C_log, lc, ld=None if C_log.dtype == np.uint16 else max(4, (C_log.shape[1 if lc == "row" else 0] + 3) // 4 * 4))
+    else:
+        C, ldc = None, 0
+    return oracle.gemm(M, N, K, A, lda, la, B, ldb, lb, alpha, beta, C, ldc, lc)
+
+
+@pytest.mark.parametrize("la,lb", [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col")])
+def test_identity_left_is_exact(la, lb):
+    B = bf16(48, 37, seed=11)
+    C = run(eye_bf16(48), B, la, lb)
+    assert np.array_equal(C, val(B))
+
+
+@pytest.mark.parametrize("la,lb", [("row", "col"), ("col", "row")])
+def test_identity_right_is_exact(la, lb):
+    A = bf16(29, 40, seed=12)
+    C = run(A, eye_bf16(40), la, lb)
+    assert np.array_equal(C, val(A))
+
+
+def test_permutation_left_permutes_rows():
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(32)
+    assert not np.array_equal(perm, np.argsort(perm))  # not an involution: a transpose would show
+    B = bf16(32, 21, seed=13)
+    C = run(perm_bf16(perm), B, "row", "col")
+    assert np.array_equal(C, val(B)[perm])
+
+
+def test_permutation_right_permutes_columns():
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(24)
+    A = bf16(19, 24, seed=14)
+    P = perm_bf16(perm)                  # (A P)[:, j] = A[:, q] where P[q, j] = 1
+    C = run(A, P, "col", "row")
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(24)
+    assert np.array_equal(C, val(A)[:, inv])
+
+
+def test_all_ones_gives_column_sums():
+    K = 256
+    B = bf16(K, 33, seed=15)
+    C = run(bf16(7, K, seed=0, dist="ones"), B, "row", "row")
+    sums = np.array([math.fsum(col) for col in val(B).T])  # correctly rounded sums
+    for i in range(7):
+        assert np.array_equal(C[i], sums)
+
+
+def test_rank_one_is_exact_outer_product():
+    u = bf16(23, 1, seed=16)
+    v = bf16(1, 31, seed=17)
+    C = run(u, v, "row", "col", alpha=0.5)
+    assert np.array_equal(C, 0.5 * np.outer(val(u)[:, 0], val(v)[0]))
+
+
+def test_alpha_zero_gives_scaled_c_exactly():
+    A = bf16(9, 16, seed=18)
+    B = bf16(16, 11, seed=19)
+    Cin = bf16(9, 11, seed=20)
+    C = run(A, B, alpha=0.0, beta=-0.75, C_log=Cin)
+    assert np.array_equal(C, -0.75 * val(Cin))
+
+
+def test_beta_zero_never_reads_c():
+    A = bf16(9, 16, seed=21)
+    B = bf16(16, 11, seed=22)
+    nan_c = np.full((9, 11), np.nan, dtype=np.float32)
+    C = run(A, B, beta=0.0, C_log=nan_c)
+    assert np.isfinite(C).all()
+
+
+def test_fp32_c_in_is_read_as_float32():
+    A = bf16(5, 8, seed=23)
+    B = bf16(8, 6, seed=24)
+    Cin = inputs.f32_matrix(5, 6, "normal", seed=25)
+    ref = run(A, B) + 2.0 * Cin.astype(np.float64)
+    got = run(A, B, beta=2.0, C_log=Cin)
+    assert np.allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def exact_gemm(A_log, B_log, alpha, beta, C_log):
+    Av = val(A_log)
+    Bv = val(B_log)
+    M, K = Av.shape
+    N = Bv.shape[1]
+    out = [[None] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = sum((Fraction(float(Av[i, k])) * Fraction(float(Bv[k, j])) for k in range(K)), Fraction(0))
+            r = Fraction(alpha) * s
+            if beta != 0.0:
+                r += Fraction(beta) * Fraction(float(val(C_log)[i, j]))
+            out[i][j] = r
+    return out
+
+
+@pytest.mark.parametrize("trial", range(12))
+def test_brute_force_rational_tiny(trial):
+    rng = np.random.default_rng(100 + trial)
+    M, N, K = (int(x) for x in rng.integers(1, 9, size=3))
+    la, lb, lc = (("row", "col")[int(b)] for b in rng.integers(0, 2, size=3))
+    alpha = float(rng.choice([1.0, -0.5, 0.375, 3.0]))
+    beta = float(rng.choice([0.0, 1.0, 0.5, -2.0]))
+    A = bf16(M, K, seed=200 + trial)
+    B = bf16(K, N, seed=300 + trial)
+    Cin = bf16(M, N, seed=400 + trial)
+    got = run(A, B, la, lb, alpha, beta, Cin, lc)
+    ref = exact_gemm(A, B, alpha, beta, Cin)
+    Av, Bv, Cv = val(A), val(B), val(Cin)
+    for i in range(M):
+        for j in range(N):
+            mag = abs(alpha) * float(np.abs(Av[i]) @ np.abs(Bv[:, j])) + abs(beta) * abs(Cv[i, j])
+            bound = (K + 2) * 2.0 ** -53 * mag
+            assert abs(Fraction(float(got[i, j])) - ref[i][j]) <= Fraction(bound)
+
+
+@pytest.mark.parametrize("shape", [(100, 70, 300), (64, 129, 257)])
+def test_matches_numpy_float64_matmul(shape):
+    M, N, K = shape
+    A = bf16(M, K, seed=31, dist="uniform")
+    B = bf16(K, N, seed=32, dist="uniform")
+    got = run(A, B, "row", "col")
+    ref = val(A) @ val(B)
+    scale = np.abs(val(A)) @ np.abs(val(B))
+    assert np.all(np.abs(got - ref) <= 2 * K * 2.0 ** -53 * scale)
+
+
+def test_layouts_give_identical_bits():
+    A = bf16(37, 45, seed=41)
+    B = bf16(45, 29, seed=42)
+    outs = [run(A, B, la, lb) for la in ("row", "col") for lb in ("row", "col")]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+def test_padded_leading_dimension_is_respected():
+    A = bf16(13, 10, seed=43)
+    B = bf16(10, 7, seed=44)
+    Ab, lda = inputs.store(A, "row", ld=24)
+    Ab[:, 10:] = inputs.f64_to_bf16_bits(np.full((13, 14), 1e4))  # garbage in the padding
+    Bb, ldb = inputs.store(B, "col", ld=16)
+    got = oracle.gemm(13, 7, 10, Ab, lda, "row", Bb, ldb, "col")
+    assert np.array_equal(got, run(A, B))
+
+
+def test_entries_match_full_product_and_rationals():
+    A = bf16(6, 5, seed=51)
+    B = bf16(5, 4, seed=52)
+    Cin = bf16(6, 4, seed=53)
+    Ab, lda = inputs.store(A, "row")
+    Bb, ldb = inputs.store(B, "row")
+    Cb, ldc = inputs.store(Cin, "row")
+    rows = np.array([0, 5, 3, 2, 5])
+    cols = np.array([0, 3, 1, 2, 0])
+    got = oracle.gemm_entries(rows, cols, 5, Ab, lda, "row", Bb, ldb, "row", 1.5, 0.5, Cb, ldc)
+    ref = exact_gemm(A, B, 1.5, 0.5, Cin)
+    for t in range(len(rows)):
+        assert abs(Fraction(float(got[t])) - ref[rows[t]][cols[t]]) <= Fraction(1, 2 ** 40)
+    full = oracle.gemm(6, 4, 5, Ab, lda, "row", Bb, ldb, "row", 1.5, 0.5, Cb, ldc)
+    assert np.array_equal(got, full[rows, cols])
+
+
+def test_attention_scores_with_identity_keys_returns_queries():
+    d = 16
+    Q = np.stack([bf16(10, d, seed=60 + b) for b in range(3)])
+    Kmat = np.stack([eye_bf16(d)] * 3)
+    S = oracle.attention_scores(Q, Kmat)
+    assert np.array_equal(S, val(Q))
+
+
+def test_attention_scores_rational_and_per_batch():
+    Q = np.stack([bf16(4, 6, seed=70 + b) for b in range(2)])
+    Kmat = np.stack([bf16(5, 6, seed=80 + b) for b in range(2)])
+    S = oracle.attention_scores(Q, Kmat)
+    for b in range(2):
+        ref = exact_gemm(Q[b], Kmat[b].T.copy(), 1.0, 0.0, None)
+        for i in range(4):
+            for j in range(5):
+                assert abs(Fraction(float(S[b, i, j])) - ref[i][j]) <= Fraction(1, 2 ** 40)
+    # batches must not mix: swapping the key batches swaps the results
+    S2 = oracle.attention_scores(Q, Kmat[::-1].copy())
+    assert not np.array_equal(S2[0], S[0])
+
+
+def test_empty_shapes():
+    A = np.zeros((0, 8), dtype=np.uint16)
+    B = bf16(8, 8, seed=90)
+    assert oracle.gemm(0, 8, 8, A, 8, "row", B, 8, "row").shape == (0, 8)
+    z = oracle.gemm(3, 4, 0, np.zeros((3, 8), np.uint16), 8, "row", np.zeros((0, 8), np.uint16), 8, "row")
+    assert np.array_equal(z, np.zeros((3, 4)))
