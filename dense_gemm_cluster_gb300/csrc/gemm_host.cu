@@ -1,0 +1,571 @@
+// Host side of the C ABI declared in include/densegemm.h: option and argument
+// validation, launch planning, TMA descriptor encoding, and the persistent
+// cluster launch ("Clusters, distributed shared memory & cluster launch
+// control", section "Thread-block clusters": the cluster shape travels as a
+// launch attribute of cudaLaunchKernelEx).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "densegemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxSmemPerCta = 232448;        // 227 KB opt-in shared memory per block on sm_103
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+thread_local std::string g_thread_error;
+
+gemm_status_t fail(std::string* sink, gemm_status_t s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    (sink ? *sink : g_thread_error) = buf;
+    return s;
+}
+
+bool pow2_le8(int v) { return v == 1 || v == 2 || v == 4 || v == 8; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// One operand as the kernel sees it: a 3-D tensor (inner, outer, batch).
+struct Operand {
+    const void* ptr;
+    int64_t ld;       // elements between consecutive outer indices
+    int64_t stride;   // elements between batches
+    bool mn_major;    // inner index runs along M (A) / N (B) rather than K
+};
+
+struct Resolved {
+    gemm_plan_t pub;
+    int64_t M, N, K;         // problem as launched (after the C^T transpose)
+    int mcast_a, mcast_b;
+    bool a_mn, b_mn;
+    int out_f32;
+};
+
+// Everything gemm_run decides before touching the GPU.
+gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, int64_t batch,
+                      int sm_count, Resolved& r, std::string* err) {
+    if (o.mode != GEMM_MODE_UNICAST && o.mode != GEMM_MODE_MCAST)
+        return fail(err, GEMM_ERR_INVALID_ARG, "mode must be GEMM_MODE_UNICAST or GEMM_MODE_MCAST");
+    if ((o.layout_a | o.layout_b | o.layout_c) & ~1)
+        return fail(err, GEMM_ERR_INVALID_ARG, "layouts must be GEMM_ROW_MAJOR or GEMM_COL_MAJOR");
+    if (o.out_type != GEMM_OUT_BF16 && o.out_type != GEMM_OUT_F32)
+        return fail(err, GEMM_ERR_INVALID_ARG, "out_type must be GEMM_OUT_BF16 or GEMM_OUT_F32");
+    if (o.cta_group != 1 && o.cta_group != 2)
+        return fail(err, GEMM_ERR_UNSUPPORTED, "cta_group must be 1 or 2");
+    if (!pow2_le8(o.cluster_m) || !pow2_le8(o.cluster_n) || o.cluster_m * o.cluster_n > 8)
+        return fail(err, GEMM_ERR_UNSUPPORTED, "cluster %dx%d: each extent 1/2/4/8 and at most 8 CTAs",
+                    o.cluster_m, o.cluster_n);
+    if (o.block_n != 0 && o.block_n != 128 && o.block_n != 256)
+        return fail(err, GEMM_ERR_UNSUPPORTED, "block_n must be 0, 128 or 256");
+    if (o.group_m < 0 || o.max_clusters < 0 || o.stages < 0)
+        return fail(err, GEMM_ERR_INVALID_ARG, "group_m, max_clusters and stages must be >= 0");
+    if (M < 0 || N < 0 || K < 0 || batch < 0)
+        return fail(err, GEMM_ERR_INVALID_ARG, "negative size");
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) || batch >= (1ll << 31))
+        return fail(err, GEMM_ERR_INVALID_ARG, "every dimension must be below 2^31");
+
+    const bool swap = o.layout_c == GEMM_COL_MAJOR;
+    const int cm = swap ? o.cluster_n : o.cluster_m;
+    const int cn = swap ? o.cluster_m : o.cluster_n;
+    const int G = o.cta_group;
+    if (G == 2 && (cm & 1))
+        return fail(err, GEMM_ERR_UNSUPPORTED,
+                    "cta_group 2 pairs CTAs along M: the cluster extent along M%s must be even",
+                    swap ? " (cluster_n, since column-major C swaps M and N)" : "");
+    int ma = o.mode == GEMM_MODE_MCAST ? (swap ? o.mcast_b : o.mcast_a) : 0;
+    int mb = o.mode == GEMM_MODE_MCAST ? (swap ? o.mcast_a : o.mcast_b) : 0;
+    const int gA = ma ? cn : 1;
+    const int gB = mb ? cm / G : 1;
+    if (gA == 1) ma = 0;
+    if (gB == 1) mb = 0;
+
+    const int BN = o.block_n ? o.block_n : 256;
+    const int a_bytes = dgc::BLOCK_M * dgc::BLOCK_K * 2;
+    const int b_bytes = (BN / G) * dgc::BLOCK_K * 2;
+    const int stage_bytes = a_bytes + b_bytes;
+    // 1024 for aligning the dynamic base, the epilogue staging, then per stage a
+    // full and an empty barrier, plus 5 barriers, the TMEM address and the abort flag.
+    const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 5 * 8 + 16;
+    int S = o.stages;
+    const int max_s = (kMaxSmemPerCta - fixed) / (stage_bytes + 16);
+    if (S == 0) S = max_s < 8 ? max_s : 8;
+    if (S < 2 || S > max_s || S > 16)
+        return fail(err, GEMM_ERR_UNSUPPORTED, "stages %d: between 2 and %d fit in shared memory", S, max_s);
+
+    r.M = swap ? N : M;
+    r.N = swap ? M : N;
+    r.K = K;
+    r.mcast_a = ma;
+    r.mcast_b = mb;
+    // A' = B^T when swapped: B row-major (N contiguous) becomes an M'-contiguous A'.
+    const int la = swap ? (o.layout_b == GEMM_ROW_MAJOR ? GEMM_COL_MAJOR : GEMM_ROW_MAJOR) : o.layout_a;
+    const int lb = swap ? (o.layout_a == GEMM_ROW_MAJOR ? GEMM_COL_MAJOR : GEMM_ROW_MAJOR) : o.layout_b;
+    r.a_mn = la == GEMM_COL_MAJOR;   // A' (M' x K) column-major: M' contiguous
+    r.b_mn = lb == GEMM_ROW_MAJOR;   // B' (K x N') row-major: N' contiguous
+    r.out_f32 = o.out_type == GEMM_OUT_F32;
+
+    gemm_plan_t& p = r.pub;
+    memset(&p, 0, sizeof p);
+    p.block_m = dgc::BLOCK_M;
+    p.block_n = BN;
+    p.block_k = dgc::BLOCK_K;
+    p.stages = S;
+    p.smem_bytes = fixed + S * (stage_bytes + 16);
+    p.cluster_m = cm;
+    p.cluster_n = cn;
+    p.cta_group = G;
+    p.group_a = gA;
+    p.group_b = gB;
+    p.transposed = swap ? 1 : 0;
+    const int64_t tm = ceil_div(r.M, (int64_t)cm * dgc::BLOCK_M);
+    const int64_t tn = ceil_div(r.N, (int64_t)cn * BN);
+    p.tiles = tm * tn * batch;
+    int64_t clusters = sm_count / (cm * cn);
+    if (o.max_clusters > 0 && o.max_clusters < clusters) clusters = o.max_clusters;
+    if (p.tiles < clusters) clusters = p.tiles;
+    p.clusters = clusters;
+    const int64_t k_pad = ceil_div(K, dgc::BLOCK_K) * dgc::BLOCK_K;
+    p.l2_to_sm_operand_bytes = p.tiles * cm * cn * k_pad * 2 * (dgc::BLOCK_M / gA + (BN / G) / gB);
+    return GEMM_OK;
+}
+
+template <int BN, int G>
+void* kernel_ptr() {
+    return reinterpret_cast<void*>(&dgc::dgc_gemm_kernel<BN, G>);
+}
+
+void* pick_kernel(int BN, int G) {
+    if (BN == 256) return G == 1 ? kernel_ptr<256, 1>() : kernel_ptr<256, 2>();
+    return G == 1 ? kernel_ptr<128, 1>() : kernel_ptr<128, 2>();
+}
+
+// K == 0: C <- beta * C (zero when beta == 0, without reading C).
+__global__ void scale_c_kernel(void* C, int64_t rows, int64_t cols, int64_t ldc, int64_t stride,
+                               int64_t batch, int f32, float beta) {
+    const int64_t per = rows * cols;
+    const int64_t total = per * batch;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i / per, rc = i - b * per, r = rc / cols, c = rc - r * cols;
+        const int64_t off = b * stride + r * ldc + c;
+        if (f32) {
+            float* p = static_cast<float*>(C) + off;
+            *p = beta == 0.0f ? 0.0f : beta * *p;
+        } else {
+            uint16_t* p = static_cast<uint16_t*>(C) + off;
+            float v = beta == 0.0f ? 0.0f : beta * __uint_as_float((uint32_t)*p << 16);
+            *p = (uint16_t)(dgc::pack_bf16x2(v, 0.0f) & 0xFFFFu);
+        }
+    }
+}
+
+}  // namespace
+
+struct gemm_handle_s {
+    gemm_options_t opt;
+    int device = 0;
+    int sm_count = 0;
+    unsigned int* d_status = nullptr;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::string err;
+    void* stage_ptr[3] = {nullptr, nullptr, nullptr};
+    size_t stage_cap[3] = {0, 0, 0};
+    int64_t launches = 0;
+    bool smem_set[2][2] = {{false, false}, {false, false}};
+    int occ_key[2][2][9];       // cached max active clusters per (BN, G, cluster size)
+};
+
+static const char* kStatusNames[] = {
+    "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_ALIGNMENT",
+    "GEMM_ERR_CUDA", "GEMM_ERR_DEVICE_TIMEOUT", "GEMM_ERR_NOT_SM103"};
+
+extern "C" const char* gemm_status_string(gemm_status_t s) {
+    if ((int)s < 0 || (int)s >= (int)(sizeof kStatusNames / sizeof kStatusNames[0])) return "GEMM_ERR_UNKNOWN";
+    return kStatusNames[s];
+}
+
+extern "C" const char* gemm_last_error(gemm_handle_t h) {
+    return h ? h->err.c_str() : g_thread_error.c_str();
+}
+
+extern "C" void gemm_options_default(gemm_options_t* o) {
+    if (!o) return;
+    memset(o, 0, sizeof *o);
+    o->mode = GEMM_MODE_UNICAST;
+    o->cluster_m = 1;
+    o->cluster_n = 1;
+    o->cta_group = 1;
+    o->layout_a = GEMM_ROW_MAJOR;
+    o->layout_b = GEMM_COL_MAJOR;
+    o->layout_c = GEMM_ROW_MAJOR;
+    o->out_type = GEMM_OUT_BF16;
+}
+
+extern "C" gemm_status_t gemm_plan(const gemm_options_t* opt, int64_t M, int64_t N, int64_t K,
+                                   int64_t batch, int sm_count, gemm_plan_t* plan) {
+    if (!opt || !plan || sm_count <= 0)
+        return fail(nullptr, GEMM_ERR_INVALID_ARG, "gemm_plan needs options, a plan and sm_count > 0");
+    Resolved r;
+    gemm_status_t s = resolve(*opt, M, N, K, batch, sm_count, r, nullptr);
+    if (s == GEMM_OK) *plan = r.pub;
+    return s;
+}
+
+static bool world_is_multi_gpu() {
+    const char* w = getenv("WORLD_SIZE");
+    return w && atoi(w) > 1;
+}
+
+extern "C" gemm_status_t gemm_create(gemm_handle_t* out, const gemm_options_t* opt, int device) {
+    if (!out || !opt) return fail(nullptr, GEMM_ERR_INVALID_ARG, "gemm_create needs out and opt");
+    *out = nullptr;
+    Resolved r;
+    gemm_status_t s = resolve(*opt, 0, 0, 0, 1, 1, r, nullptr);
+    if (s != GEMM_OK) return s;
+    if (opt->mode == GEMM_MODE_MCAST && (opt->mcast_a || opt->mcast_b) && world_is_multi_gpu())
+        return fail(nullptr, GEMM_ERR_UNSUPPORTED,
+                    "cluster multicast is single-GPU only; WORLD_SIZE > 1 requires unicast or the pair MMA");
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess)
+        return fail(nullptr, GEMM_ERR_CUDA, "cudaGetDeviceProperties(%d): %s", device, cudaGetErrorString(e));
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(nullptr, GEMM_ERR_NOT_SM103, "device %d is sm_%d%d; this library is built for sm_103a",
+                    device, prop.major, prop.minor);
+    gemm_handle_s* h = new gemm_handle_s();
+    h->opt = *opt;
+    if (h->opt.wait_timeout_ns == 0) h->opt.wait_timeout_ns = kDefaultTimeoutNs;
+    h->device = device;
+    h->sm_count = prop.multiProcessorCount;
+    memset(h->occ_key, 0, sizeof h->occ_key);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(device);
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        cudaSetDevice(prev);
+        delete h;
+        return fail(nullptr, GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    e = cudaMalloc(&h->d_status, 16);
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 16);
+    cudaSetDevice(prev);
+    if (e != cudaSuccess) {
+        delete h;
+        return fail(nullptr, GEMM_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+    }
+    *out = h;
+    return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_destroy(gemm_handle_t h) {
+    if (!h) return GEMM_OK;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(h->device);
+    if (h->d_status) cudaFree(h->d_status);
+    for (int i = 0; i < 3; ++i)
+        if (h->stage_ptr[i]) cudaFree(h->stage_ptr[i]);
+    cudaSetDevice(prev);
+    delete h;
+    return GEMM_OK;
+}
+
+extern "C" int64_t gemm_launch_count(gemm_handle_t h) { return h ? h->launches : -1; }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Encodes a 3-D tiled map (inner, outer, batch) with the 128-byte swizzle.
+static gemm_status_t encode_map(gemm_handle_s* h, CUtensorMap* map, CUtensorMapDataType dt, int esize,
+                                const void* ptr, int64_t inner, int64_t outer, int64_t batch,
+                                int64_t ld, int64_t stride, uint32_t box_inner, uint32_t box_outer,
+                                const char* what) {
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)batch};
+    int64_t bstride = batch > 1 ? stride : ((ld * outer + 15) / 16) * 16;
+    if (bstride <= 0) bstride = 16;
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(bstride * esize)};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res = h->encode(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS)
+        return fail(&h->err, GEMM_ERR_INVALID_ARG,
+                    "cuTensorMapEncodeTiled(%s) failed with %d (dims %lld x %lld x %lld, ld %lld, stride %lld)",
+                    what, (int)res, (long long)inner, (long long)outer, (long long)batch, (long long)ld,
+                    (long long)stride);
+    return GEMM_OK;
+}
+
+static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                              int64_t strideA, const void* B, int64_t ldb, int64_t strideB, void* C,
+                              int64_t ldc, int64_t strideC, int64_t batch, float alpha, float beta,
+                              void* stream_v) {
+    if (!h) return fail(nullptr, GEMM_ERR_INVALID_ARG, "null handle");
+    const gemm_options_t& o = h->opt;
+    Resolved r;
+    gemm_status_t s = resolve(o, M, N, K, batch, h->sm_count, r, &h->err);
+    if (s != GEMM_OK) return s;
+    if (M == 0 || N == 0 || batch == 0) return GEMM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const int esc = o.out_type == GEMM_OUT_F32 ? 4 : 2;
+
+    // ---- argument checks (user's view: A M x K, B K x N, C M x N)
+    if (!C) return fail(&h->err, GEMM_ERR_INVALID_ARG, "C is null");
+    if (K > 0 && (!A || !B)) return fail(&h->err, GEMM_ERR_INVALID_ARG, "A or B is null");
+    const int64_t a_inner = o.layout_a == GEMM_ROW_MAJOR ? K : M;
+    const int64_t a_outer = o.layout_a == GEMM_ROW_MAJOR ? M : K;
+    const int64_t b_inner = o.layout_b == GEMM_ROW_MAJOR ? N : K;
+    const int64_t b_outer = o.layout_b == GEMM_ROW_MAJOR ? K : N;
+    const int64_t c_inner = o.layout_c == GEMM_ROW_MAJOR ? N : M;
+    const int64_t c_outer = o.layout_c == GEMM_ROW_MAJOR ? M : N;
+    if (ldc < c_inner || ldc < 1) return fail(&h->err, GEMM_ERR_INVALID_ARG, "ldc %lld < %lld", (long long)ldc, (long long)c_inner);
+    if (!aligned16(C) || (ldc * esc) % 16)
+        return fail(&h->err, GEMM_ERR_ALIGNMENT, "C must be 16-byte aligned with ldc*%d a multiple of 16", esc);
+    if (batch > 1) {
+        if ((strideC * esc) % 16 || strideC < ldc * c_outer)
+            return fail(&h->err, strideC < ldc * c_outer ? GEMM_ERR_INVALID_ARG : GEMM_ERR_ALIGNMENT,
+                        "strideC must be a multiple of 16 bytes and keep batches of C apart");
+    }
+    if (K > 0) {
+        if (lda < a_inner || lda < 1) return fail(&h->err, GEMM_ERR_INVALID_ARG, "lda %lld < %lld", (long long)lda, (long long)a_inner);
+        if (ldb < b_inner || ldb < 1) return fail(&h->err, GEMM_ERR_INVALID_ARG, "ldb %lld < %lld", (long long)ldb, (long long)b_inner);
+        if (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16)
+            return fail(&h->err, GEMM_ERR_ALIGNMENT,
+                        "A and B must be 16-byte aligned with lda*2 and ldb*2 multiples of 16");
+        if (batch > 1 && ((strideA * 2) % 16 || (strideB * 2) % 16 || strideA < 0 || strideB < 0))
+            return fail(&h->err, GEMM_ERR_ALIGNMENT, "strideA*2 and strideB*2 must be non-negative multiples of 16");
+    }
+    (void)a_outer;
+    (void)b_outer;
+
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    struct Restore {
+        int d, p;
+        ~Restore() { if (d != p) cudaSetDevice(p); }
+    } restore{h->device, prev};
+
+    if (K == 0) {
+        const int64_t total = M * N * batch;
+        const int threads = 256;
+        const int64_t blocks = total / threads + 1 < 4096 ? total / threads + 1 : 4096;
+        // Row-major view of C: rows x cols with leading dimension ldc.
+        scale_c_kernel<<<(unsigned)blocks, threads, 0, stream>>>(C, c_outer, c_inner, ldc, strideC, batch,
+                                                                 o.out_type == GEMM_OUT_F32, beta);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "scale launch: %s", cudaGetErrorString(e));
+        h->launches++;
+        return GEMM_OK;
+    }
+
+    // ---- operands as launched (column-major C computes C^T = B^T A^T)
+    Operand opA{A, lda, strideA, o.layout_a == GEMM_COL_MAJOR};
+    Operand opB{B, ldb, strideB, o.layout_b == GEMM_ROW_MAJOR};
+    if (r.pub.transposed) {
+        // A' = B^T (N x K): B row-major has N contiguous -> M'-major.
+        // B' = A^T (K x M): A row-major has K contiguous -> K-major.
+        Operand a2{B, ldb, strideB, o.layout_b == GEMM_ROW_MAJOR};
+        Operand b2{A, lda, strideA, o.layout_a == GEMM_COL_MAJOR};
+        opA = a2;
+        opB = b2;
+    }
+    const gemm_plan_t& pl = r.pub;
+    const int BN = pl.block_n, G = pl.cta_group;
+    const int gA = pl.group_a, gB = pl.group_b;
+
+    CUtensorMap tmA, tmB, tmC;
+    if (!opA.mn_major)
+        s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.K, r.M, batch, opA.ld, opA.stride,
+                       64, dgc::BLOCK_M / gA, "A");
+    else
+        s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.M, r.K, batch, opA.ld, opA.stride,
+                       64, dgc::BLOCK_K / gA, "A");
+    if (s != GEMM_OK) return s;
+    if (!opB.mn_major)
+        s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.K, r.N, batch, opB.ld, opB.stride,
+                       64, (BN / G) / gB, "B");
+    else
+        s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.N, r.K, batch, opB.ld, opB.stride,
+                       64, dgc::BLOCK_K / gB, "B");
+    if (s != GEMM_OK) return s;
+    s = encode_map(h, &tmC, r.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, esc,
+                   C, r.N, r.M, batch, ldc, strideC, r.out_f32 ? 32 : 64, 32, "C");
+    if (s != GEMM_OK) return s;
+
+    dgc::KernelParams kp;
+    memset(&kp, 0, sizeof kp);
+    kp.M = (int)r.M;
+    kp.N = (int)r.N;
+    kp.K = (int)r.K;
+    kp.batch = (int)batch;
+    kp.num_kb = (int)ceil_div(r.K, dgc::BLOCK_K);
+    kp.cx = pl.cluster_m;
+    kp.cy = pl.cluster_n;
+    kp.mcast_a = r.mcast_a;
+    kp.mcast_b = r.mcast_b;
+    kp.a_mn_major = opA.mn_major;
+    kp.b_mn_major = opB.mn_major;
+    kp.out_f32 = r.out_f32;
+    kp.tiles_m = (int)ceil_div(r.M, (int64_t)pl.cluster_m * dgc::BLOCK_M);
+    kp.tiles_n = (int)ceil_div(r.N, (int64_t)pl.cluster_n * BN);
+    kp.total_tiles = pl.tiles;
+    kp.group_m = o.group_m > 0 ? o.group_m : 8;
+    kp.stages = pl.stages;
+    kp.debug_flags = o.debug_flags;
+    kp.alpha = alpha;
+    kp.beta = beta;
+    kp.c_in = C;
+    kp.ldc = ldc;
+    kp.stride_c = strideC;
+    kp.status = h->d_status;
+    kp.timeout_ns = o.wait_timeout_ns;
+
+    void* fn = pick_kernel(BN, G);
+    const int bi = BN == 256 ? 1 : 0, gi = G - 1;
+    if (!h->smem_set[bi][gi]) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerCta);
+        if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+        h->smem_set[bi][gi] = true;
+    }
+    const int cs = pl.cluster_m * pl.cluster_n;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(dgc::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int& occ = h->occ_key[bi][gi][cs];
+    if (occ == 0) {
+        cfg.gridDim = dim3((unsigned)(cs * (h->sm_count / cs)), 1, 1);
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+        if (e != cudaSuccess || n <= 0)
+            return fail(&h->err, GEMM_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s (n=%d)",
+                        cudaGetErrorString(e), n);
+        occ = n;
+    }
+    int64_t clusters = pl.clusters < occ ? pl.clusters : occ;
+    cfg.gridDim = dim3((unsigned)(clusters * cs), 1, 1);
+    void* args[] = {&tmA, &tmB, &tmC, &kp};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "cudaLaunchKernelEx: %s", cudaGetErrorString(e));
+    h->launches++;
+    return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                  const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
+                                  void* stream) {
+    return run_impl(h, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, alpha, beta, stream);
+}
+
+extern "C" gemm_status_t gemm_run_strided_batched(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                                  const void* A, int64_t lda, int64_t strideA, const void* B,
+                                                  int64_t ldb, int64_t strideB, void* C, int64_t ldc,
+                                                  int64_t strideC, int64_t batch, float alpha, float beta,
+                                                  void* stream) {
+    return run_impl(h, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch, alpha, beta, stream);
+}
+
+static gemm_status_t ensure_stage(gemm_handle_t h, int i, size_t bytes) {
+    if (h->stage_cap[i] >= bytes) return GEMM_OK;
+    if (h->stage_ptr[i]) cudaFree(h->stage_ptr[i]);
+    h->stage_ptr[i] = nullptr;
+    h->stage_cap[i] = 0;
+    cudaError_t e = cudaMalloc(&h->stage_ptr[i], bytes);
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "staging buffer: %s", cudaGetErrorString(e));
+    h->stage_cap[i] = bytes;
+    return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                                       int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                                       float alpha, float beta, void* stream_v) {
+    if (!h) return fail(nullptr, GEMM_ERR_INVALID_ARG, "null handle");
+    if (M < 0 || N < 0 || K < 0) return fail(&h->err, GEMM_ERR_INVALID_ARG, "negative size");
+    if (M == 0 || N == 0) return GEMM_OK;
+    const gemm_options_t& o = h->opt;
+    const int esc = o.out_type == GEMM_OUT_F32 ? 4 : 2;
+    auto footprint = [](int64_t outer, int64_t inner, int64_t ld) -> int64_t {
+        return outer == 0 || inner == 0 ? 0 : (outer - 1) * ld + inner;
+    };
+    const int64_t a_n = o.layout_a == GEMM_ROW_MAJOR ? footprint(M, K, lda) : footprint(K, M, lda);
+    const int64_t b_n = o.layout_b == GEMM_ROW_MAJOR ? footprint(K, N, ldb) : footprint(N, K, ldb);
+    const int64_t c_n = o.layout_c == GEMM_ROW_MAJOR ? footprint(M, N, ldc) : footprint(N, M, ldc);
+    if (!C || (K > 0 && (!A || !B))) return fail(&h->err, GEMM_ERR_INVALID_ARG, "null host pointer");
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    struct Restore {
+        int d, p;
+        ~Restore() { if (d != p) cudaSetDevice(p); }
+    } restore{h->device, prev};
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    gemm_status_t s;
+    if ((s = ensure_stage(h, 0, (size_t)(a_n * 2) + 16)) != GEMM_OK) return s;
+    if ((s = ensure_stage(h, 1, (size_t)(b_n * 2) + 16)) != GEMM_OK) return s;
+    if ((s = ensure_stage(h, 2, (size_t)(c_n * esc) + 16)) != GEMM_OK) return s;
+    cudaError_t e = cudaSuccess;
+    if (K > 0) {
+        e = cudaMemcpyAsync(h->stage_ptr[0], A, (size_t)a_n * 2, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(h->stage_ptr[1], B, (size_t)b_n * 2, cudaMemcpyHostToDevice, stream);
+    }
+    if (e == cudaSuccess && beta != 0.0f)
+        e = cudaMemcpyAsync(h->stage_ptr[2], C, (size_t)c_n * esc, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "host-to-device copy: %s", cudaGetErrorString(e));
+    s = run_impl(h, M, N, K, h->stage_ptr[0], lda, 0, h->stage_ptr[1], ldb, 0, h->stage_ptr[2], ldc, 0, 1,
+                 alpha, beta, stream_v);
+    if (s != GEMM_OK) return s;
+    e = cudaMemcpyAsync(C, h->stage_ptr[2], (size_t)c_n * esc, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
+    return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_query_status(gemm_handle_t h, void* stream_v) {
+    if (!h) return fail(nullptr, GEMM_ERR_INVALID_ARG, "null handle");
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    struct Restore {
+        int d, p;
+        ~Restore() { if (d != p) cudaSetDevice(p); }
+    } restore{h->device, prev};
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_v));
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+    unsigned int w[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(w, h->d_status, sizeof w, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (w[0] == 0) return GEMM_OK;
+    static const char* roles[] = {"none", "producer waiting for a free stage", "MMA waiting for stage bytes",
+                                  "MMA waiting for a free accumulator", "epilogue waiting for an accumulator",
+                                  "teardown waiting for in-flight MMAs"};
+    const char* role = w[0] < 6 ? roles[w[0]] : "unknown";
+    fail(&h->err, GEMM_ERR_DEVICE_TIMEOUT, "bounded wait expired: %s (stage/buffer %u, CTA %u, tile %d)", role,
+         w[1], w[2], (int)w[3]);
+    cudaMemset(h->d_status, 0, 16);
+    return GEMM_ERR_DEVICE_TIMEOUT;
+}

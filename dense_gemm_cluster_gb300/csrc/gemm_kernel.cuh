@@ -1,0 +1,497 @@
+// Persistent, cluster-launched, warp-specialised GEMM for sm_103a.
+//
+//   C[b] <- alpha * A[b] * B[b] + beta * C[b]      bf16 A/B, fp32 accumulate in TMEM
+//
+// One CTA owns 128 rows of C (BLOCK_M). A cluster of cx * cy CTAs (cx along M,
+// cy along N) covers a "cluster tile" of cx*128 rows by cy*BN columns. Roles:
+//
+//   warp 0      producer: TMA loads of A/B k-blocks into an S-stage ring
+//   warp 1      TMEM allocation; MMA issue (one elected lane; with the pair MMA
+//               only the pair's even CTA issues)
+//   warps 2..5  epilogue: TMEM -> registers -> (alpha, beta) -> shared -> TMA store
+//
+// Operand sharing ("Hopper TMA Multicast 深度解析与实测", sections
+// 核心架构认知 / 深度机制剖析 / 工程总结; "Clusters, distributed shared memory &
+// cluster launch control", sections "TMA multicast" and "Two CTAs, one MMA"):
+//   * A multicast: the cy CTAs of a cluster row share A. CTA with row index
+//     idxA loads rows [idxA*128/cy, (idxA+1)*128/cy) of the A tile and delivers
+//     them to every CTA of the row with one multicast.
+//   * B multicast: the CTAs of a cluster column that hold the same B columns
+//     (all cx of them, or the cx/2 CTAs of equal parity with the pair MMA)
+//     split and multicast the B tile the same way.
+//   * Before each load the issuer arms, for every receiving CTA, the barrier
+//     that will count those bytes (its own or a peer's, through mapa), so no
+//     barrier can complete before every delivery it waits for is announced.
+//   * Pair MMA (G = 2): CTAs 2p and 2p+1 of a cluster column form a pair; the
+//     even CTA issues tcgen05.mma.cta_group::2 with M = 256 (A rows split across
+//     the pair) and N = BN (B columns split across the pair). Every TMA load of
+//     the pair signals the even CTA's barrier.
+//   * Stage reuse: each consumer commits its release of stage s to the "empty"
+//     barrier of every CTA that writes into its shared memory, so an issuer
+//     only overwrites a stage once all its receivers are done with it.
+//
+// Tile order is a static persistent stride over cluster tiles ("Clusters,
+// distributed shared memory & cluster launch control", section "The second
+// wall"), rastered in bands of group_m cluster-rows so that co-running
+// clusters share A and B tiles in L2.
+//
+// Every wait is bounded by wait_timeout_ns of %globaltimer; on expiry the
+// thread records a status word in global memory, raises a CTA-wide abort flag
+// and its role stops, so the kernel always returns.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+#include "ptx.cuh"
+
+namespace dgc {
+
+constexpr int BLOCK_M = 128;
+constexpr int BLOCK_K = 64;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF_BYTES = 4096;                              // 32 rows x 128 bytes
+constexpr int EPI_SMEM_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;    // double-buffered per warp
+constexpr int BOX_BYTES = 8192;                                  // 64 rows x 128 bytes
+
+// Error codes written to status[0] by a wait that ran out.
+enum : uint32_t {
+    ERR_NONE = 0,
+    ERR_WAIT_EMPTY = 1,      // producer waiting for a stage to be released
+    ERR_WAIT_FULL = 2,       // MMA waiting for a stage's bytes
+    ERR_WAIT_TMEM_EMPTY = 3, // MMA waiting for the epilogue to free an accumulator
+    ERR_WAIT_TMEM_FULL = 4,  // epilogue waiting for an accumulator
+    ERR_WAIT_DRAIN = 5,      // teardown waiting for in-flight MMAs
+};
+
+struct KernelParams {
+    int M, N, K;             // problem (after any transpose for column-major C)
+    int batch;
+    int num_kb;              // ceil(K / 64), >= 1
+    int cx, cy;              // cluster extent along M / N (CTAs)
+    int mcast_a, mcast_b;
+    int a_mn_major, b_mn_major;
+    int out_f32;
+    int tiles_m, tiles_n;    // cluster tiles along M / N per batch
+    long long total_tiles;   // tiles_m * tiles_n * batch
+    int group_m;
+    int stages;
+    int debug_flags;
+    float alpha, beta;
+    const void* c_in;        // C (read when beta != 0)
+    long long ldc, stride_c; // elements
+    unsigned int* status;    // 4 words: code, detail, block, tile
+    unsigned long long timeout_ns;
+};
+
+struct TileCoord {
+    int b, ctm, ctn;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const KernelParams& p, long long t) {
+    const long long per_batch = (long long)p.tiles_m * p.tiles_n;
+    TileCoord c;
+    c.b = (int)(t / per_batch);
+    const long long r = t - (long long)c.b * per_batch;
+    const long long in_group = (long long)p.group_m * p.tiles_n;
+    const int group = (int)(r / in_group);
+    const int first_m = group * p.group_m;
+    const int gsz = min(p.group_m, p.tiles_m - first_m);
+    const int local = (int)(r - (long long)group * in_group);
+    c.ctm = first_m + local % gsz;
+    c.ctn = local / gsz;
+    return c;
+}
+
+__device__ __noinline__ void report_timeout(const KernelParams& p, uint32_t code, uint32_t detail,
+                                            long long tile) {
+    if (atomicCAS(p.status, 0u, code) == 0u) {
+        p.status[1] = detail;
+        p.status[2] = blockIdx.x;
+        p.status[3] = (unsigned int)tile;
+        __threadfence();
+    }
+}
+
+// Bounded wait on phase `parity` of the barrier at `bar`. Returns false (after
+// recording the reason unless another role already aborted) when the budget is
+// spent or the CTA is aborting.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const KernelParams& p,
+                                             volatile int* abort_flag, uint32_t code, uint32_t detail,
+                                             long long tile) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            report_timeout(p, code, detail, tile);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Bitmask of the CTAs of cluster row `rx` (same A rows), ranks rx + cx*y.
+__device__ __forceinline__ uint32_t row_mask(int rx, int cx, int cy) {
+    uint32_t m = 0;
+    for (int y = 0; y < cy; ++y) m |= 1u << (rx + cx * y);
+    return m;
+}
+// Bitmask of the CTAs of cluster column `ry` holding the same B columns:
+// every x (G = 1) or every x of the same parity as rx (G = 2).
+template <int G>
+__device__ __forceinline__ uint32_t col_mask(int rx, int ry, int cx) {
+    uint32_t m = 0;
+    for (int x = (G == 2 ? (rx & 1) : 0); x < cx; x += G) m |= 1u << (x + cx * ry);
+    return m;
+}
+
+// Loads this CTA's slice (index `slice` of `parts`) of one operand k-block.
+// K-major operand (rows x 64 K, 128-byte rows): slice by rows.
+// MN-major operand (64 K rows per 64-wide MN box): slice every box by K rows.
+template <int G>
+__device__ __forceinline__ void load_operand_slice(const CUtensorMap* tmap, uint32_t dst_tile,
+                                                   uint32_t bar, int mn_major, int rows, int mn0,
+                                                   int k0, int b, int slice, int parts, uint32_t mask) {
+    const bool mcast = parts > 1;
+    if (!mn_major) {
+        const int r = rows / parts;
+        const uint32_t dst = dst_tile + (uint32_t)(slice * r * 128);
+        const int y = mn0 + slice * r;
+        if (G == 1) {
+            if (mcast) tma_load_3d_mcast(dst, tmap, bar, k0, y, b, (uint16_t)mask);
+            else       tma_load_3d(dst, tmap, bar, k0, y, b);
+        } else {
+            if (mcast) tma_load_3d_pair_mcast(dst, tmap, bar, k0, y, b, (uint16_t)mask);
+            else       tma_load_3d_pair(dst, tmap, bar, k0, y, b);
+        }
+    } else {
+        const int kr = BLOCK_K / parts;
+        for (int box = 0; box < rows / 64; ++box) {
+            const uint32_t dst = dst_tile + (uint32_t)(box * BOX_BYTES + slice * kr * 128);
+            const int x = mn0 + box * 64;
+            const int y = k0 + slice * kr;
+            if (G == 1) {
+                if (mcast) tma_load_3d_mcast(dst, tmap, bar, x, y, b, (uint16_t)mask);
+                else       tma_load_3d(dst, tmap, bar, x, y, b);
+            } else {
+                if (mcast) tma_load_3d_pair_mcast(dst, tmap, bar, x, y, b, (uint16_t)mask);
+                else       tma_load_3d_pair(dst, tmap, bar, x, y, b);
+            }
+        }
+    }
+}
+
+template <int BN, int G>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
+    constexpr int BN_CTA = BN / G;                      // B columns held per CTA
+    constexpr uint32_t A_BYTES = BLOCK_M * BLOCK_K * 2;
+    constexpr uint32_t B_BYTES = BN_CTA * BLOCK_K * 2;
+    constexpr uint32_t TMEM_COLS = 2 * BN;              // two accumulators
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+    static_assert(BN_CTA % 64 == 0, "B slab must be whole 64-column boxes");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = p.stages;
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + S * A_BYTES;
+    uint8_t* sEpi = sB + S * B_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + EPI_SMEM_BYTES);
+    uint64_t* full_bar = bars;
+    uint64_t* empty_bar = bars + S;
+    uint64_t* tfull_bar = bars + 2 * S;
+    uint64_t* tempty_bar = bars + 2 * S + 2;
+    uint64_t* drain_bar = bars + 2 * S + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cx = p.cx, cy = p.cy;
+    const int rx = (int)rank % cx;
+    const int ry = (int)rank / cx;
+    const uint32_t leader = (G == 2) ? (rank & ~1u) : rank;
+
+    // Sharing groups of this CTA.
+    const int gA = p.mcast_a ? cy : 1;
+    const int idxA = p.mcast_a ? ry : 0;
+    const uint32_t maskA = p.mcast_a ? row_mask(rx, cx, cy) : (1u << rank);
+    const int gB = p.mcast_b ? cx / G : 1;
+    const int idxB = p.mcast_b ? rx / G : 0;
+    const uint32_t maskB = p.mcast_b ? col_mask<G>(rx, ry, cx) : (1u << rank);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), (uint32_t)(G * (gA + gB)));
+            mbar_init(smem_u32(&empty_bar[s]), (uint32_t)(gA + gB - 1));
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&tfull_bar[i]), 1);
+            mbar_init(smem_u32(&tempty_bar[i]), (uint32_t)(G * EPI_WARPS));
+        }
+        mbar_init(smem_u32(drain_bar), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<G>(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish<G>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const long long first_tile = cluster_id_x();
+    const long long tile_stride = num_clusters_x();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            bool extra_tx = (p.debug_flags & 1) != 0;
+            const uint32_t sliceA = A_BYTES / gA;
+            const uint32_t sliceB = B_BYTES / gB;
+            for (long long t = first_tile; ok && t < p.total_tiles; t += tile_stride) {
+                const TileCoord tc = tile_coord(p, t);
+                const int m0 = (tc.ctm * cx + rx) * BLOCK_M;
+                const int nB0 = (tc.ctn * cy + ry) * BN + (G == 2 ? (rx & 1) * BN_CTA : 0);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag,
+                                      ERR_WAIT_EMPTY, (uint32_t)stage, t)) { ok = false; break; }
+                    const uint32_t full_local = smem_u32(&full_bar[stage]);
+                    // Arm every receiver's counting barrier before issuing.
+                    for (uint32_t m = maskA; m; m &= m - 1) {
+                        const uint32_t d = (uint32_t)(__ffs(m) - 1);
+                        mbar_arrive_expect_tx_cluster(mapa(full_local, G == 2 ? (d & ~1u) : d), sliceA);
+                    }
+                    for (uint32_t m = maskB; m; m &= m - 1) {
+                        const uint32_t d = (uint32_t)(__ffs(m) - 1);
+                        mbar_arrive_expect_tx_cluster(mapa(full_local, G == 2 ? (d & ~1u) : d), sliceB);
+                    }
+                    if (extra_tx) {
+                        // Test hook: announce bytes that never come; the MMA's
+                        // bounded wait on this stage must run out.
+                        asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;"
+                                     :: "r"(mapa(full_local, leader)), "r"(16u) : "memory");
+                        extra_tx = false;
+                    }
+                    const uint32_t tma_bar = (G == 2) ? mapa(full_local, leader) : full_local;
+                    const int k0 = kb * BLOCK_K;
+                    load_operand_slice<G>(&tmA, smem_u32(sA + stage * A_BYTES), tma_bar, p.a_mn_major,
+                                          BLOCK_M, m0, k0, tc.b, idxA, gA, maskA);
+                    load_operand_slice<G>(&tmB, smem_u32(sB + stage * B_BYTES), tma_bar, p.b_mn_major,
+                                          BN_CTA, nB0, k0, tc.b, idxB, gB, maskB);
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Drain: wait until every stage this CTA filled has been released by
+            // all of its receivers, so no remote arrival targets this CTA after exit.
+            for (int i = 0; ok && i < S; ++i) {
+                if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag,
+                                  ERR_WAIT_EMPTY, (uint32_t)stage, -1)) break;
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && rank == leader) {
+            constexpr uint32_t UMMA_M = BLOCK_M * G;
+            const uint32_t idesc = instr_desc_bf16(UMMA_M, BN, p.a_mn_major != 0, p.b_mn_major != 0);
+            // Everyone who writes into this pair's shared memory gets the release.
+            uint32_t empty_mask = maskA | maskB;
+            if (G == 2) {
+                const int px = rx ^ 1;
+                const uint32_t pr = (uint32_t)(px + cx * ry);
+                empty_mask |= (p.mcast_a ? row_mask(px, cx, cy) : (1u << pr)) |
+                              (p.mcast_b ? col_mask<G>(px, ry, cx) : (1u << pr));
+            }
+            const bool local_only = (empty_mask == (1u << rank));
+            const uint32_t a_kstep = p.a_mn_major ? 16u * 128u : 32u;   // bytes per 16-element K step
+            const uint32_t b_kstep = p.b_mn_major ? 16u * 128u : 32u;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t local_tile = 0;
+            bool ok = true;
+            for (long long t = first_tile; ok && t < p.total_tiles; t += tile_stride, ++local_tile) {
+                const uint32_t acc = local_tile & 1u;
+                const uint32_t acc_phase = (local_tile >> 1) & 1u;
+                if (!wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p, abort_flag,
+                                  ERR_WAIT_TMEM_EMPTY, acc, t)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(smem_u32(&full_bar[stage]), phase, p, abort_flag,
+                                      ERR_WAIT_FULL, (uint32_t)stage, t)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+                    const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BLOCK_K / 16; ++k) {
+                        const uint64_t adesc = smem_desc_sw128(a_base + k * a_kstep, p.a_mn_major != 0);
+                        const uint64_t bdesc = smem_desc_sw128(b_base + k * b_kstep, p.b_mn_major != 0);
+                        mma_bf16<G>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    const uint32_t eb = smem_u32(&empty_bar[stage]);
+                    if (local_only) mma_commit<G>(eb);
+                    else            mma_commit_mcast<G>(eb, (uint16_t)empty_mask);
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                const uint32_t fb = smem_u32(&tfull_bar[acc]);
+                if (G == 1) mma_commit<G>(fb);
+                else        mma_commit_mcast<G>(fb, (uint16_t)(3u << leader));
+            }
+            if (*abort_flag) {
+                // Let issued MMAs finish before the accumulators are freed.
+                mma_commit<G>(smem_u32(drain_bar));
+                wait_bounded(smem_u32(drain_bar), 0, p, abort_flag, ERR_WAIT_DRAIN, 0, -1);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                           // TMEM lane quadrant of this warp
+        const int ew = warp - 2;                          // staging buffers of this warp
+        const uint32_t stage_base = smem_u32(sEpi + ew * 2 * EPI_BUF_BYTES);
+        uint8_t* stage_ptr = sEpi + ew * 2 * EPI_BUF_BYTES;
+        const int CW = p.out_f32 ? 32 : 64;               // columns per 128-byte store row
+        const int chunks = BN / CW;
+        const uint32_t tempty_target = (G == 2) ? mapa(smem_u32(&tempty_bar[0]), leader)
+                                                : smem_u32(&tempty_bar[0]);
+        const bool use_beta = p.beta != 0.0f;
+        uint32_t local_tile = 0;
+        uint32_t buf = 0;
+        for (long long t = first_tile; t < p.total_tiles; t += tile_stride, ++local_tile) {
+            const uint32_t acc = local_tile & 1u;
+            const uint32_t acc_phase = (local_tile >> 1) & 1u;
+            if (!wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, p, abort_flag,
+                              ERR_WAIT_TMEM_FULL, acc, t)) break;
+            tc_fence_after();
+            const TileCoord tc = tile_coord(p, t);
+            const int m0 = (tc.ctm * cx + rx) * BLOCK_M;
+            const int n0 = (tc.ctn * cy + ry) * BN;
+            const int row = m0 + q * 32 + lane;           // global row this thread stores
+            const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            for (int c = 0; c < chunks; ++c) {
+                const int col0 = n0 + c * CW;
+                float v[64];
+                {
+                    uint32_t r[32];
+                    tmem_ld_32cols(t_row + c * CW, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                }
+                if (!p.out_f32) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(t_row + c * CW + 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
+                }
+                if (c == chunks - 1) {
+                    // All of this accumulator is in registers: hand it back.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_target + acc * 8u);
+                }
+                // alpha * acc + beta * C_in, in fp32.
+                if (use_beta) {
+                    const bool row_ok = row < p.M;
+                    if (p.out_f32) {
+                        const float* src = static_cast<const float*>(p.c_in) + (long long)tc.b * p.stride_c +
+                                           (long long)row * p.ldc + col0;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float ci = (row_ok && col0 + i < p.N) ? src[i] : 0.0f;
+                            v[i] = fmaf(p.alpha, v[i], p.beta * ci);
+                        }
+                    } else {
+                        const uint16_t* src = static_cast<const uint16_t*>(p.c_in) + (long long)tc.b * p.stride_c +
+                                              (long long)row * p.ldc + col0;
+                        if (row_ok && col0 + 64 <= p.N) {
+                            const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint4 w = s4[j];
+                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const float lo = __uint_as_float(ws[h] << 16);
+                                    const float hi = __uint_as_float(ws[h] & 0xFFFF0000u);
+                                    v[8 * j + 2 * h] = fmaf(p.alpha, v[8 * j + 2 * h], p.beta * lo);
+                                    v[8 * j + 2 * h + 1] = fmaf(p.alpha, v[8 * j + 2 * h + 1], p.beta * hi);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 64; ++i) {
+                                const float ci = (row_ok && col0 + i < p.N)
+                                                     ? __uint_as_float((uint32_t)src[i] << 16) : 0.0f;
+                                v[i] = fmaf(p.alpha, v[i], p.beta * ci);
+                            }
+                        }
+                    }
+                } else if (p.alpha != 1.0f) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] *= p.alpha;
+                }
+                // Pack one 128-byte row per thread.
+                uint32_t w[32];
+                if (p.out_f32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                }
+                // The buffer about to be written was last used two stores ago.
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                uint8_t* rowp = stage_ptr + buf * EPI_BUF_BYTES + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
+                    uint4* dst = reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4));
+                    *dst = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&tmC, stage_base + buf * EPI_BUF_BYTES, col0, m0 + q * 32, tc.b);
+                    bulk_commit_group();
+                }
+                buf ^= 1u;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (*abort_flag) {
+        // Give any copy still in flight time to land before the CTA exits.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 50000ull) { }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<G>(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace dgc

@@ -1,0 +1,224 @@
+"""Python binding of the C ABI in include/densegemm.h (argument marshalling only).
+
+Every function named like the C entry point takes the same arguments, with
+pointers given as ints or as tensors (their ``data_ptr()``), and returns the
+C status code. All arithmetic runs in libdensegemm.so; importing this module
+fails loudly if the library has not been built (there is no other code path).
+
+``Gemm`` wraps a handle for callers holding torch tensors: it derives sizes and
+leading dimensions from the tensors and raises ``GemmError`` on a bad status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+_LIB_PATH = _build.LIB_PATH
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libdensegemm.so is not built ({_LIB_PATH}); run "
+        "`python -m dense_gemm_cluster_gb300.build` or __graft_entry__.build()")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED = 2
+GEMM_ERR_ALIGNMENT = 3
+GEMM_ERR_CUDA = 4
+GEMM_ERR_DEVICE_TIMEOUT = 5
+GEMM_ERR_NOT_SM103 = 6
+
+GEMM_ROW_MAJOR = 0
+GEMM_COL_MAJOR = 1
+GEMM_OUT_BF16 = 0
+GEMM_OUT_F32 = 1
+GEMM_MODE_UNICAST = 0
+GEMM_MODE_MCAST = 1
+GEMM_DEBUG_EXTRA_TX = 1
+
+
+class gemm_options_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "mode", "mcast_a", "mcast_b", "cluster_m", "cluster_n", "cta_group", "layout_a", "layout_b",
+        "layout_c", "out_type", "block_n", "stages", "max_clusters", "group_m")] + [
+        ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_int)]
+
+
+class gemm_plan_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "block_m", "block_n", "block_k", "stages", "smem_bytes", "cluster_m", "cluster_n", "cta_group",
+        "group_a", "group_b", "transposed")] + [
+        ("tiles", ctypes.c_int64), ("clusters", ctypes.c_int64), ("l2_to_sm_operand_bytes", ctypes.c_int64)]
+
+
+_i64, _i32, _f32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+_OPT_P = ctypes.POINTER(gemm_options_t)
+
+_lib.gemm_options_default.argtypes = [_OPT_P]
+_lib.gemm_options_default.restype = None
+_lib.gemm_create.argtypes = [ctypes.POINTER(_vp), _OPT_P, _i32]
+_lib.gemm_create.restype = _i32
+_lib.gemm_run.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp]
+_lib.gemm_run.restype = _i32
+_lib.gemm_run_strided_batched.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
+                                          _vp, _i64, _i64, _i64, _f32, _f32, _vp]
+_lib.gemm_run_strided_batched.restype = _i32
+_lib.gemm_run_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp]
+_lib.gemm_run_host.restype = _i32
+_lib.gemm_query_status.argtypes = [_vp, _vp]
+_lib.gemm_query_status.restype = _i32
+_lib.gemm_plan.argtypes = [_OPT_P, _i64, _i64, _i64, _i64, _i32, ctypes.POINTER(gemm_plan_t)]
+_lib.gemm_plan.restype = _i32
+_lib.gemm_status_string.argtypes = [_i32]
+_lib.gemm_status_string.restype = ctypes.c_char_p
+_lib.gemm_last_error.argtypes = [_vp]
+_lib.gemm_last_error.restype = ctypes.c_char_p
+_lib.gemm_launch_count.argtypes = [_vp]
+_lib.gemm_launch_count.restype = _i64
+_lib.gemm_destroy.argtypes = [_vp]
+_lib.gemm_destroy.restype = _i32
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):           # numpy array (host pointer)
+        return x.ctypes.data
+    raise TypeError(f"cannot take a pointer of {type(x).__name__}")
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream               # torch.cuda.Stream
+
+
+# ---------------------------------------------------------------- C-ABI names
+def gemm_options_default() -> gemm_options_t:
+    o = gemm_options_t()
+    _lib.gemm_options_default(ctypes.byref(o))
+    return o
+
+
+def gemm_create(opt: gemm_options_t, device: int = 0):
+    """Returns (status, handle); handle is an opaque int (0 on failure)."""
+    h = _vp()
+    s = _lib.gemm_create(ctypes.byref(h), ctypes.byref(opt), device)
+    return s, (h.value or 0)
+
+
+def gemm_run(h, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream=None) -> int:
+    return _lib.gemm_run(h, M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, alpha, beta, _stream(stream))
+
+
+def gemm_run_strided_batched(h, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch,
+                             alpha, beta, stream=None) -> int:
+    return _lib.gemm_run_strided_batched(h, M, N, K, _ptr(A), lda, strideA, _ptr(B), ldb, strideB, _ptr(C),
+                                         ldc, strideC, batch, alpha, beta, _stream(stream))
+
+
+def gemm_run_host(h, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream=None) -> int:
+    return _lib.gemm_run_host(h, M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, alpha, beta,
+                              _stream(stream))
+
+
+def gemm_query_status(h, stream=None) -> int:
+    return _lib.gemm_query_status(h, _stream(stream))
+
+
+def gemm_plan(opt: gemm_options_t, M, N, K, batch=1, sm_count=148):
+    """Returns (status, gemm_plan_t)."""
+    p = gemm_plan_t()
+    s = _lib.gemm_plan(ctypes.byref(opt), M, N, K, batch, sm_count, ctypes.byref(p))
+    return s, p
+
+
+def gemm_status_string(s: int) -> str:
+    return _lib.gemm_status_string(s).decode()
+
+
+def gemm_last_error(h=None) -> str:
+    return (_lib.gemm_last_error(h) or b"").decode()
+
+
+def gemm_launch_count(h) -> int:
+    return int(_lib.gemm_launch_count(h))
+
+
+def gemm_destroy(h) -> int:
+    return _lib.gemm_destroy(h)
+
+
+# ---------------------------------------------------------------- convenience
+class GemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{gemm_status_string(status)}: {message}")
+        self.status = status
+
+
+def make_options(**kw) -> gemm_options_t:
+    """gemm_options_default() with fields overridden by keyword (layouts as "row"/"col",
+    out_type as "bf16"/"f32", mode as "unicast"/"mcast")."""
+    o = gemm_options_default()
+    names = {"row": GEMM_ROW_MAJOR, "col": GEMM_COL_MAJOR, "bf16": GEMM_OUT_BF16, "f32": GEMM_OUT_F32,
+             "unicast": GEMM_MODE_UNICAST, "mcast": GEMM_MODE_MCAST}
+    for k, v in kw.items():
+        if not hasattr(o, k):
+            raise TypeError(f"gemm_options_t has no field {k!r}")
+        setattr(o, k, names.get(v, v) if isinstance(v, str) else int(v))
+    return o
+
+
+class Gemm:
+    """A handle bound to one device and one set of options."""
+
+    def __init__(self, device: int = 0, **options):
+        self.options = make_options(**options)
+        s, self.handle = gemm_create(self.options, device)
+        if s != GEMM_OK:
+            raise GemmError(s, gemm_last_error(None))
+
+    def check(self, status: int) -> None:
+        if status != GEMM_OK:
+            raise GemmError(status, gemm_last_error(self.handle))
+
+    def run(self, M, N, K, A, lda, B, ldb, C, ldc, alpha=1.0, beta=0.0, stream=None) -> None:
+        self.check(gemm_run(self.handle, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream))
+
+    def run_strided_batched(self, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch, alpha=1.0, beta=0.0,
+                            stream=None) -> None:
+        self.check(gemm_run_strided_batched(self.handle, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch,
+                                            alpha, beta, stream))
+
+    def run_host(self, M, N, K, A, lda, B, ldb, C, ldc, alpha=1.0, beta=0.0, stream=None) -> None:
+        self.check(gemm_run_host(self.handle, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream))
+
+    def query_status(self, stream=None) -> int:
+        return gemm_query_status(self.handle, stream)
+
+    @property
+    def launches(self) -> int:
+        return gemm_launch_count(self.handle)
+
+    def close(self) -> None:
+        if self.handle:
+            gemm_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,178 @@
+/*
+ * densegemm.h -- C ABI of the GB300 (sm_103a) cluster GEMM library.
+ *
+ * The operation is the tiled dense contraction
+ *
+ *     C <- alpha * A * B + beta * C          (bf16 A and B, fp32 accumulation,
+ *                                             bf16 or fp32 C)
+ *
+ * and its batched attention-score form S[b] = Q[b] * K[b]^T, which is the same
+ * call with B given column-major ("Hopper TMA Multicast 深度解析与实测", section
+ * 经典应用场景: S_i = Q_i K^T with the K tile shared by the Q-tile CTAs).
+ * How the CTAs of a thread-block cluster share operand tiles is the mode knob:
+ *
+ *   - unicast: every CTA fetches its own A and B tiles with TMA;
+ *   - multicast: one TMA load feeds every CTA of a cluster that needs the same
+ *     tile (A along a cluster row, B along a cluster column), the issuer arming
+ *     each receiver's mbarrier with the expected bytes through mapa before it
+ *     issues ("Hopper TMA Multicast 深度解析与实测", sections 深度机制剖析 and
+ *     工程总结; "Clusters, distributed shared memory & cluster launch control",
+ *     section "TMA multicast");
+ *   - cta_group 2: two CTAs of a cluster run one 256-row tcgen05 MMA, A split by
+ *     rows across the pair and B split by columns, each CTA holding its half of
+ *     the accumulator in its own tensor memory ("Clusters, distributed shared
+ *     memory & cluster launch control", section "Two CTAs, one MMA --
+ *     cta_group::2"). It combines with multicast.
+ *
+ * Work is spread by a persistent, cluster-launched kernel that walks output
+ * tiles with a static stride ("Clusters, distributed shared memory & cluster
+ * launch control", sections "Thread-block clusters" and "The second wall").
+ *
+ * Conventions for every call:
+ *   - Pointers A, B, C are DEVICE pointers owned by the caller (except in
+ *     gemm_run_host, where they are host pointers). The library never frees them.
+ *   - Sizes and leading dimensions are in elements. A row-major X has its last
+ *     index contiguous: element (r, c) at X[r*ld + c]; column-major: X[c*ld + r].
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Runs are asynchronous on it unless a call says otherwise.
+ *   - Every call returns a gemm_status_t; nothing exits, aborts or throws across
+ *     this boundary. On failure, gemm_last_error() holds a one-line reason.
+ *   - A handle is used by one host thread at a time.
+ */
+#ifndef DENSEGEMM_H
+#define DENSEGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_handle_s *gemm_handle_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,    /* a null handle/pointer, negative size, ld too small, bad enum */
+    GEMM_ERR_UNSUPPORTED = 2,    /* a mode / cluster / cta_group combination this build does not run */
+    GEMM_ERR_ALIGNMENT = 3,      /* a base pointer not 16-byte aligned, or ld/stride bytes not a multiple of 16 */
+    GEMM_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed; see gemm_last_error() */
+    GEMM_ERR_DEVICE_TIMEOUT = 5, /* a bounded in-kernel wait expired; the kernel stopped cleanly */
+    GEMM_ERR_NOT_SM103 = 6       /* the device is not compute capability 10.3 */
+} gemm_status_t;
+
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+typedef enum { GEMM_OUT_BF16 = 0, GEMM_OUT_F32 = 1 } gemm_out_t;
+typedef enum { GEMM_MODE_UNICAST = 0, GEMM_MODE_MCAST = 1 } gemm_mode_t;
+
+/* Test hook: arm 16 bytes more than the first stage will receive, so that the
+ * consumer's bounded wait must expire and report GEMM_ERR_DEVICE_TIMEOUT.
+ * Nothing faults and nothing spins without a limit. */
+#define GEMM_DEBUG_EXTRA_TX 1
+
+typedef struct {
+    int mode;           /* gemm_mode_t. UNICAST ignores mcast_a / mcast_b. */
+    int mcast_a;        /* 1: multicast each A tile to the CTAs of its cluster row (cluster_n of them) */
+    int mcast_b;        /* 1: multicast each B tile to the CTAs of its cluster column
+                           (cluster_m of them, or cluster_m / 2 pairs with cta_group 2) */
+    int cluster_m;      /* CTAs per cluster along M: 1, 2, 4 or 8 */
+    int cluster_n;      /* CTAs per cluster along N: 1, 2, 4 or 8; cluster_m*cluster_n <= 8 */
+    int cta_group;      /* 1, or 2 for the pair MMA (cluster_m must then be even) */
+    int layout_a;       /* gemm_layout_t of A (M x K) */
+    int layout_b;       /* gemm_layout_t of B (K x N) */
+    int layout_c;       /* gemm_layout_t of C (M x N) */
+    int out_type;       /* gemm_out_t: element type of C */
+    int block_n;        /* N extent of one MMA tile: 0 (auto = 256), 128 or 256 */
+    int stages;         /* shared-memory pipeline depth; 0 = as many as fit */
+    int max_clusters;   /* cap on the persistent grid, in clusters; 0 = as many as are co-resident */
+    int group_m;        /* raster band height, in cluster tiles along M; 0 = 8 */
+    uint64_t wait_timeout_ns; /* bound on every in-kernel wait; 0 = 2 s */
+    int debug_flags;    /* 0, or GEMM_DEBUG_EXTRA_TX (tests only) */
+} gemm_options_t;
+
+/* What gemm_run would launch for a given problem (host arithmetic only). */
+typedef struct {
+    int block_m;        /* rows of C per CTA (128) */
+    int block_n;        /* columns of C per MMA tile */
+    int block_k;        /* K per pipeline stage (64) */
+    int stages;         /* pipeline depth */
+    int smem_bytes;     /* dynamic shared memory per CTA */
+    int cluster_m, cluster_n;   /* after the column-major-C transpose, if any */
+    int cta_group;
+    int group_a;        /* CTAs one A fetch serves (1 = unicast) */
+    int group_b;        /* CTAs one B fetch serves */
+    int transposed;     /* 1: C column-major was computed as C^T = B^T A^T */
+    int64_t tiles;      /* cluster tiles in the whole problem (all batches) */
+    int64_t clusters;   /* persistent grid size in clusters (before the occupancy cap) */
+    int64_t l2_to_sm_operand_bytes; /* analytic TMA operand fetches for the launch */
+} gemm_plan_t;
+
+/* Default options: unicast, 1x1 cluster, cta_group 1, A row-major, B column-major,
+ * C row-major, bf16 out, everything else automatic. */
+void gemm_options_default(gemm_options_t *opt);
+
+/* Checks the options and makes a handle bound to CUDA device `device`.
+ * Fails with GEMM_ERR_NOT_SM103 off compute capability 10.3, GEMM_ERR_UNSUPPORTED
+ * for an impossible mode (cluster > 8 CTAs, odd cluster_m with cta_group 2, a
+ * multicast slice under 8 rows) and for any multicast mode when the environment
+ * variable WORLD_SIZE is above 1 (multi-GPU jobs run without cluster multicast).
+ * The handle owns a 16-byte device status word and, after gemm_run_host, staging
+ * buffers; gemm_destroy frees them. */
+gemm_status_t gemm_create(gemm_handle_t *out, const gemm_options_t *opt, int device);
+
+/* C <- alpha * op(A) * op(B) + beta * C on `stream`, asynchronously.
+ * A is M x K with leading dimension lda (layout_a), B is K x N (layout_b), C is
+ * M x N (layout_c, out_type). beta == 0 means C is not read (NaN in C does not
+ * propagate). M, N or K == 0 is valid: K == 0 gives C <- beta * C.
+ * Requirements, checked before any launch: A, B, C 16-byte aligned; lda*2,
+ * ldb*2 and ldc*sizeof(C element) multiples of 16 bytes (GEMM_ERR_ALIGNMENT);
+ * ld at least the contiguous extent; every dimension below 2^31. */
+gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                       const void *A, int64_t lda, const void *B, int64_t ldb,
+                       void *C, int64_t ldc, float alpha, float beta, void *stream);
+
+/* `batch` independent products C[i] <- alpha*A[i]*B[i] + beta*C[i], where X[i]
+ * starts strideX elements after X[i-1]. Strides must be multiples of 16 bytes;
+ * strideC must not make two outputs overlap. The attention-score form is
+ * A = Q (row-major, sq x d), B = K^T (K given row-major sk x d is B column-major
+ * with ldb = d), C = S (fp32, sq x sk). */
+gemm_status_t gemm_run_strided_batched(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                       const void *A, int64_t lda, int64_t strideA,
+                                       const void *B, int64_t ldb, int64_t strideB,
+                                       void *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                       float alpha, float beta, void *stream);
+
+/* gemm_run on HOST buffers: copies A, B (and C when beta != 0) to device staging
+ * owned by the handle, runs, copies C back, and synchronizes `stream` before
+ * returning. Host buffers may be pageable or pinned; pinned copies are faster. */
+gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                            const void *A, int64_t lda, const void *B, int64_t ldb,
+                            void *C, int64_t ldc, float alpha, float beta, void *stream);
+
+/* Synchronizes `stream`, then reads and clears the device status word.
+ * GEMM_ERR_DEVICE_TIMEOUT if a bounded wait expired in any run since the last
+ * query (gemm_last_error() then names the role, stage and CTA). */
+gemm_status_t gemm_query_status(gemm_handle_t h, void *stream);
+
+/* Host-only planning: validates `opt` and the problem as gemm_run would and
+ * fills `plan`. Needs no GPU; `sm_count` stands in for the device's SM count. */
+gemm_status_t gemm_plan(const gemm_options_t *opt, int64_t M, int64_t N, int64_t K,
+                        int64_t batch, int sm_count, gemm_plan_t *plan);
+
+/* Static string for a status code. */
+const char *gemm_status_string(gemm_status_t s);
+
+/* The last failure reason recorded on this handle (or by gemm_create / gemm_plan
+ * when h is NULL, per thread). Valid until the next call on the same handle. */
+const char *gemm_last_error(gemm_handle_t h);
+
+/* Number of GEMM kernel launches this handle has made (for launch accounting). */
+int64_t gemm_launch_count(gemm_handle_t h);
+
+/* Frees the handle and everything it owns. Safe on NULL. */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSEGEMM_H */

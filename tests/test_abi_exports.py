@@ -1,0 +1,114 @@
+"""The C-ABI library builds, loads, and exports every entry point include/densegemm.h declares.
+
+Also checks the host-only planner (no GPU needed): validation and launch plans.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_gemm_cluster_gb300 import build
+    build.build()
+    from dense_gemm_cluster_gb300 import gemm
+    return gemm
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(gemm_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "gemm_run" in names and "gemm_create" in names and len(names) >= 10
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(lib._lib, n)
+
+
+def test_status_strings(lib):
+    assert lib.gemm_status_string(0) == "GEMM_OK"
+    assert lib.gemm_status_string(5) == "GEMM_ERR_DEVICE_TIMEOUT"
+    assert lib.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def test_options_default(lib):
+    o = lib.gemm_options_default()
+    assert (o.mode, o.cluster_m, o.cluster_n, o.cta_group) == (0, 1, 1, 1)
+    assert (o.layout_a, o.layout_b, o.layout_c, o.out_type) == (0, 1, 0, 0)
+
+
+def plan(lib, M, N, K, batch=1, sm=148, **kw):
+    s, p = lib.gemm_plan(lib.make_options(**kw), M, N, K, batch, sm)
+    return s, p
+
+
+def test_plan_4096_cluster2x1(lib):
+    s, p = plan(lib, 4096, 4096, 4096, mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=1)
+    assert s == 0
+    assert (p.block_m, p.block_n, p.block_k) == (128, 256, 64)
+    assert p.group_a == 1 and p.group_b == 2          # a 2x1 cluster shares only B
+    assert p.tiles == (4096 // 256) * (4096 // 256)
+    assert p.clusters == 74
+    assert p.smem_bytes <= 232448 and p.stages == 4
+    from dense_gemm_cluster_gb300 import traffic
+    assert p.l2_to_sm_operand_bytes == traffic.l2_to_sm_operand_bytes(4096, 4096, 4096, group_b=2)
+
+
+def test_plan_pair_with_b_multicast(lib):
+    s, p = plan(lib, 8192, 8192, 8192, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1)
+    assert s == 0 and p.group_b == 2 and p.group_a == 1 and p.stages == 6
+    from dense_gemm_cluster_gb300 import traffic
+    uni = traffic.l2_to_sm_operand_bytes(8192, 8192, 8192)
+    assert uni == 2 * p.l2_to_sm_operand_bytes
+
+
+def test_plan_column_major_c_swaps_roles(lib):
+    s, p = plan(lib, 1000, 300, 64, layout_c="col", cluster_m=1, cluster_n=2, mode="mcast", mcast_a=1)
+    assert s == 0 and p.transposed == 1
+    assert (p.cluster_m, p.cluster_n) == (2, 1) and p.group_b == 2 and p.group_a == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cta_group=3), 2),
+    (dict(cluster_m=3), 2),
+    (dict(cluster_m=4, cluster_n=4), 2),
+    (dict(cta_group=2, cluster_m=1), 2),
+    (dict(block_n=96), 2),
+    (dict(stages=1), 2),
+    (dict(stages=9), 2),
+    (dict(layout_a=2), 1),
+    (dict(out_type=7), 1),
+    (dict(mode=5), 1),
+])
+def test_plan_rejects_bad_options(lib, kw, code):
+    s, _ = plan(lib, 128, 128, 128, **kw)
+    assert s == code, lib.gemm_last_error()
+    assert lib.gemm_last_error()
+
+
+def test_plan_rejects_bad_sizes(lib):
+    assert plan(lib, -1, 4, 4)[0] == 1
+    assert plan(lib, 1 << 31, 4, 4)[0] == 1
+    s, p = plan(lib, 0, 0, 0)
+    assert s == 0 and p.tiles == 0
+
+
+def test_unicast_mode_ignores_multicast_flags(lib):
+    s, p = plan(lib, 512, 512, 512, mode="unicast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2)
+    assert s == 0 and p.group_a == 1 and p.group_b == 1

@@ -1,0 +1,131 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+cta_group 1 here (unicast and cluster multicast); the pair MMA has its own file.
+"""
+import numpy as np
+import pytest
+
+from gpu_cases import Problem, assert_close, options_for, sample_positions
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def G():
+    import torch
+    from dense_gemm_cluster_gb300 import gemm
+    assert torch.cuda.is_available()
+    return gemm
+
+
+def _run(G, p, alpha=1.0, beta=0.0, **opts):
+    g = G.Gemm(0, **options_for(p, **opts))
+    try:
+        dC = p.run(g, alpha, beta)
+        assert g.query_status() == G.GEMM_OK, G.gemm_last_error(g.handle)
+        return p.result(dC)
+    finally:
+        g.close()
+
+
+def test_small_256_fp32_cluster2_multicast_b(G):
+    # 256^3, N(0,1), fp32 out, all row-major, a 2-CTA cluster sharing B by multicast
+    p = Problem(256, 256, 256, la="row", lb="row", lc="row", out="f32", seed=0)
+    got = _run(G, p, mode="mcast", mcast_b=1, cluster_m=2, cluster_n=1)
+    assert_close(got, p.reference(), 256, "f32", "256^3 mcast B")
+
+
+@pytest.mark.parametrize("la,lb", [("row", "col"), ("row", "row"), ("col", "col"), ("col", "row")])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_layouts_unicast(G, la, lb, out):
+    p = Problem(384, 512, 320, la=la, lb=lb, out=out, seed=1)
+    got = _run(G, p)
+    assert_close(got, p.reference(), 320, out, f"{la}/{lb}/{out}")
+
+
+def test_identity_is_bit_exact(G):
+    from dense_gemm_cluster_gb300 import inputs
+    p = Problem(256, 384, 256, la="row", lb="row", out="bf16", seed=2)
+    p.A_log = inputs.f64_to_bf16_bits(np.eye(256))
+    p.A, p.lda = inputs.store(p.A_log, "row")
+    got = _run(G, p)
+    assert np.array_equal(got, inputs.bf16_bits_to_f32(p.B_log).astype(np.float64))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (17, 130, 257), (130, 17, 64), (257, 257, 17),
+                                   (129, 300, 130), (1, 513, 65), (300, 1, 200)])
+@pytest.mark.parametrize("lc", ["row", "col"])
+def test_ragged_shapes(G, M, N, K, lc):
+    p = Problem(M, N, K, la="row", lb="row", lc=lc, out="bf16", seed=3)
+    got = _run(G, p)
+    assert_close(got, p.reference(), K, "bf16", f"{M}x{N}x{K} C {lc}")
+
+
+@pytest.mark.parametrize("alpha,beta,out", [(0.5, 0.0, "bf16"), (1.0, 1.0, "bf16"), (-2.0, 0.5, "f32"),
+                                            (0.0, -1.5, "bf16"), (1.0, 0.5, "f32")])
+def test_alpha_beta(G, alpha, beta, out):
+    p = Problem(300, 600, 192, out=out, beta=beta, seed=4)
+    got = _run(G, p, alpha, beta)
+    assert_close(got, p.reference(alpha, beta), 192, out, f"alpha={alpha} beta={beta}")
+
+
+@pytest.mark.parametrize("cm,cn,ma,mb", [(2, 1, 0, 1), (1, 2, 1, 0), (2, 2, 1, 1), (4, 1, 0, 1),
+                                         (1, 4, 1, 0), (4, 2, 1, 1), (2, 4, 1, 1), (8, 1, 0, 1),
+                                         (2, 1, 0, 0), (2, 2, 0, 0)])
+@pytest.mark.parametrize("bn", [128, 256])
+def test_cluster_modes_match_oracle_and_unicast_bitwise(G, cm, cn, ma, mb, bn):
+    p = Problem(1000, 1100, 448, la="row", lb="col", out="bf16", seed=5)
+    uni = _run(G, p, block_n=bn)
+    got = _run(G, p, mode="mcast", mcast_a=ma, mcast_b=mb, cluster_m=cm, cluster_n=cn, block_n=bn)
+    assert_close(got, p.reference(), 448, "bf16", f"cluster {cm}x{cn} mcast A{ma} B{mb}")
+    # multicast moves the same operand bytes: the product is bit-identical
+    assert np.array_equal(got, uni)
+
+
+@pytest.mark.parametrize("lb", ["row", "col"])
+def test_multicast_mn_major_operands(G, lb):
+    p = Problem(520, 700, 256, la="col", lb=lb, out="f32", seed=6)
+    got = _run(G, p, mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2)
+    assert_close(got, p.reference(), 256, "f32", f"mn-major mcast lb={lb}")
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4])
+def test_persistent_loop_and_stages(G, stages):
+    # a handful of clusters walking many tiles, with a shallow ring
+    p = Problem(1024, 1536, 640, seed=7)
+    got = _run(G, p, max_clusters=3, stages=stages, mode="mcast", mcast_b=1, cluster_m=2)
+    assert_close(got, p.reference(), 640, "bf16", f"persistent stages={stages}")
+
+
+def test_k_zero_scales_c(G):
+    import torch
+    from dense_gemm_cluster_gb300 import inputs
+    g = G.Gemm(0, out_type="f32", layout_b="row")
+    C = torch.randn(40, 48, device="cuda")
+    ref = (0.5 * C).cpu().numpy()
+    g.run(40, 48, 0, None, 8, None, 48, C, 48, 1.0, 0.5)
+    assert g.query_status() == G.GEMM_OK
+    assert np.array_equal(C.cpu().numpy(), ref)
+    C.fill_(float("nan"))
+    g.run(40, 48, 0, None, 8, None, 48, C, 48, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert (C == 0).all().item()
+    g.close()
+
+
+def test_gemm_4096_sampled(G):
+    # 4096^3, U(-1,1), A row-major, B column-major, bf16 out, 2x1 cluster multicast A and B
+    p = Problem(4096, 4096, 4096, la="row", lb="col", out="bf16", dist="uniform", seed=0)
+    g = G.Gemm(0, **options_for(p, mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=1))
+    dC = p.run(g)
+    assert g.query_status() == G.GEMM_OK
+    got = p.result(dC)
+    rows, cols = sample_positions(4096, 4096, 3000)
+    ref = p.reference_entries(rows, cols)
+    scale = np.max(np.abs(ref))
+    err = np.max(np.abs(got[rows, cols] - ref)) / scale
+    assert err <= 1e-2 * np.sqrt(4096 / 256), err
+    # every output is finite and of the size an N(0, K/9) sum predicts
+    assert np.isfinite(got).all()
+    assert 0.5 < np.std(got) / np.sqrt(4096 / 9.0) < 1.5
+    g.close()
