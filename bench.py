@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the cluster GEMM on GB300: GEMM TFLOP/s, % of dense-BF16 peak,
+and L2->SM operand bytes against unicast.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+One step is one gemm_run over the workload (default: GEMM 4096^3, bf16 in,
+bf16 out, 2x1 cluster multicasting A and B). Inputs are seeded synthetic
+matrices resident in HBM; L2 is flushed (a 512 MB write) before every timed
+step and each step is timed alone with CUDA events on the launching stream.
+Prints one JSON line (rank 0).
+
+--impl reference times the CPU oracle (fp64 triple loop, OpenMP) on a bounded
+sample of the same workload: the method's plain definition, not a GPU program.
+Under torchrun every rank runs the workload on its own GPU (weak scaling, no
+collective on the data path; cluster multicast is turned off when more than
+one GPU takes part).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from dense_gemm_cluster_gb300 import inputs, traffic  # noqa: E402
+from dense_gemm_cluster_gb300.workloads import DEFAULT, WORKLOADS, Workload  # noqa: E402
+
+METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense-BF16 peak; L2→SM bytes vs unicast"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ["dense_gemm_cluster_gb300/csrc/gemm_kernel.cuh", "dense_gemm_cluster_gb300/csrc/ptx.cuh",
+                  "dense_gemm_cluster_gb300/csrc/gemm_host.cu"]
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def aggregate(dist, elapsed_s: float, units: float, device=None):
+    """(max elapsed over ranks, sum of units over ranks): the whole-job clock and work."""
+    if dist is None:
+        return elapsed_s, units
+    import torch
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- peaks, clocks, profiles
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            recs = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = recs.get(workload)
+    if not rec or rec.get("kernel_sha") != kernel_source_hash():
+        return None
+    return rec
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)            # first sample lands before the timed region starts
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- inputs on the device
+class DeviceProblem:
+    """The workload's operands, generated on the host from the seed and copied to HBM once."""
+
+    def __init__(self, w: Workload, device, seed: int = 0):
+        import numpy as np
+        import torch
+        self.w = w
+        if w.batch > 1:
+            A_log = inputs.bf16_matrix(w.batch * w.M, w.K, w.dist, seed + inputs.STREAM_A, w.scale)
+            B_log = inputs.bf16_matrix(w.batch * w.N, w.K, w.dist, seed + inputs.STREAM_B, w.scale)
+            assert w.layout_a == "row" and w.layout_b == "col" and w.layout_c == "row"
+            self.A_host, self.lda, self.sA = A_log, w.K, w.M * w.K
+            self.B_host, self.ldb, self.sB = B_log, w.K, w.N * w.K
+            self.ldc, self.sC = w.N, w.M * w.N
+        else:
+            self.A_host, self.lda = inputs.store(inputs.bf16_matrix(w.M, w.K, w.dist, seed + inputs.STREAM_A,
+                                                                    w.scale), w.layout_a)
+            self.B_host, self.ldb = inputs.store(inputs.bf16_matrix(w.K, w.N, w.dist, seed + inputs.STREAM_B,
+                                                                    w.scale), w.layout_b)
+            self.sA = self.sB = self.sC = 0
+            self.ldc = w.N if w.layout_c == "row" else w.M
+        esc = 4 if w.out == "f32" else 2
+        c_elems = (w.batch * w.M * w.N)
+        if w.beta != 0.0:
+            if w.out == "bf16":
+                C_log = inputs.bf16_matrix(w.M, w.N, w.c_dist, seed + inputs.STREAM_C)
+            else:
+                C_log = inputs.f32_matrix(w.M, w.N, w.c_dist, seed + inputs.STREAM_C)
+            self.C_host, self.ldc = inputs.store(C_log, w.layout_c)
+        else:
+            self.C_host = None
+        self.A = torch.from_numpy(self.A_host.view(np.int16)).to(device)
+        self.B = torch.from_numpy(self.B_host.view(np.int16)).to(device)
+        cdt = torch.float32 if w.out == "f32" else torch.int16
+        if self.C_host is not None:
+            self.C_init = torch.from_numpy(self.C_host.view(np.int16) if w.out == "bf16" else self.C_host).to(device)
+            self.C = self.C_init.clone()
+        else:
+            self.C_init = None
+            self.C = torch.empty(c_elems, dtype=cdt, device=device)
+        self.c_bytes = c_elems * esc
+
+
+def run_once(g, p: DeviceProblem, stream):
+    w = p.w
+    if w.batch > 1:
+        g.run_strided_batched(w.M, w.N, w.K, p.A, p.lda, p.sA, p.B, p.ldb, p.sB, p.C, p.ldc, p.sC, w.batch,
+                              w.alpha, w.beta, stream)
+    else:
+        g.run(w.M, w.N, w.K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc, w.alpha, w.beta, stream)
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_rate(w: Workload, budget_s: float, seed: int = 0):
+    """Times the CPU oracle on the first R output rows of (the first batch of) the workload.
+
+    Returns (TFLOP/s, seconds, rows, threads). R is chosen from a short
+    calibration run so the timed sample takes about budget_s seconds.
+    """
+    import oracle
+    assert w.layout_a == "row"
+    A_full = inputs.bf16_matrix(w.M, w.K, w.dist, seed + inputs.STREAM_A, w.scale)
+    if w.batch > 1:
+        B_buf = inputs.bf16_matrix(w.N, w.K, w.dist, seed + inputs.STREAM_B, w.scale)   # K rows = B col-major
+        ldb, lb = w.K, "col"
+    else:
+        B_buf, ldb = inputs.store(inputs.bf16_matrix(w.K, w.N, w.dist, seed + inputs.STREAM_B, w.scale),
+                                  w.layout_b)
+        lb = w.layout_b
+    C_in = None
+    ldc = 0
+    if w.beta != 0.0:
+        C_log = (inputs.bf16_matrix(w.M, w.N, w.c_dist, seed + inputs.STREAM_C) if w.out == "bf16"
+                 else inputs.f32_matrix(w.M, w.N, w.c_dist, seed + inputs.STREAM_C))
+        C_in, ldc = inputs.store(C_log, "row")
+
+    def timed(rows):
+        A = A_full[:rows]
+        Cs = C_in[:rows] if C_in is not None else None
+        t0 = time.perf_counter()
+        oracle.gemm(rows, w.N, w.K, A, w.K, "row", B_buf, ldb, lb, w.alpha, w.beta, Cs, ldc, "row")
+        return time.perf_counter() - t0
+
+    per_row_flops = 2.0 * w.N * w.K
+    r0 = max(1, min(w.M, int(1e9 / per_row_flops)))
+    t0 = timed(r0)
+    rate = r0 * per_row_flops / max(t0, 1e-6)
+    rows = max(1, min(w.M, int(rate * budget_s / per_row_flops)))
+    t = timed(rows)
+    return rows * per_row_flops / t / 1e12, t, rows, oracle.num_threads()
+
+
+# ---------------------------------------------------------------- arms
+def bench_reference(args, w: Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    # calibrate the per-step sample once (untimed)
+    _, _, rows, threads = oracle_rate(w, per_step)
+    A_full = inputs.bf16_matrix(rows, w.K, w.dist, inputs.STREAM_A, w.scale)
+    if w.batch > 1:
+        B_buf, ldb, lb = inputs.bf16_matrix(w.N, w.K, w.dist, inputs.STREAM_B, w.scale), w.K, "col"
+    else:
+        B_buf, ldb = inputs.store(inputs.bf16_matrix(w.K, w.N, w.dist, inputs.STREAM_B, w.scale), w.layout_b)
+        lb = w.layout_b
+    C_in, ldc = None, 0
+    if w.beta != 0.0:
+        C_log = (inputs.bf16_matrix(rows, w.N, w.c_dist, inputs.STREAM_C) if w.out == "bf16"
+                 else inputs.f32_matrix(rows, w.N, w.c_dist, inputs.STREAM_C))
+        C_in, ldc = inputs.store(C_log, "row")
+    for _ in range(args.warmup):
+        oracle.gemm(rows, w.N, w.K, A_full, w.K, "row", B_buf, ldb, lb, w.alpha, w.beta, C_in, ldc, "row")
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm(rows, w.N, w.K, A_full, w.K, "row", B_buf, ldb, lb, w.alpha, w.beta, C_in, ldc, "row")
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / total / 1e12
+    sample = f"rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K}) per step, of the {w.M}x{w.N}x{w.K}" + \
+             (f" x{w.batch} batch" if w.batch > 1 else "") + " workload"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch,
+                   "description": "fp64 CPU oracle (plain triple loop, OpenMP over rows): " + w.description},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args, w: Workload):
+    import torch
+    world, rank, local = dist_env()
+    dist = init_dist(world, "nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from dense_gemm_cluster_gb300 import gemm
+
+    opts = dict(w.options)
+    if world > 1:
+        # cluster multicast stays off when several GPUs take part
+        opts["mode"] = "unicast"
+    g = gemm.Gemm(local, layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out, **opts)
+    s, plan = gemm.gemm_plan(g.options, w.M, w.N, w.K, w.batch, torch.cuda.get_device_properties(device).multi_processor_count)
+    g.check(s)
+    uni_opts = gemm.make_options(layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out,
+                                 block_n=plan.block_n)
+    _, uni_plan = gemm.gemm_plan(uni_opts, w.M, w.N, w.K, w.batch, 148)
+
+    p = DeviceProblem(w, device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    for _ in range(max(3, args.warmup)):
+        run_once(g, p, stream)
+    g.check(g.query_status(stream))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = g.launches
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))                      # evicts the operands from L2
+            starts[i].record(stream)
+            run_once(g, p, stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - wall0
+    barrier(dist)
+    launches = g.launches - launches0
+    g.check(g.query_status(stream))
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    local_s = sum(step_ms) / 1e3
+    elapsed, units = aggregate(dist, local_s, float(w.flops) * args.steps, device)
+    value = units / elapsed / 1e12
+    ms_per_step = 1e3 * elapsed / args.steps
+
+    peaks, peaks_kind = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    avg_launch_s = local_s / args.steps
+    achieved = w.flops / avg_launch_s / 1e12
+    traffic_rec = recorded_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_rec["dram_bytes"] if traffic_rec else None,
+                "peak_source": f"bf16_tflops (burst) of {peaks_kind}",
+                "algorithmic_flops_per_launch": w.flops,
+                "hbm_gbs_at_min_bytes": w.min_hbm_bytes() / avg_launch_s / 1e9}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "out": w.out,
+                   "layouts": f"A {w.layout_a}, B {w.layout_b}, C {w.layout_c}", "alpha": w.alpha,
+                   "beta": w.beta, "mode": opts, "cta_group": plan.cta_group, "block": [plan.block_m, plan.block_n,
+                                                                                        plan.block_k],
+                   "stages": plan.stages, "cluster": [plan.cluster_m, plan.cluster_n],
+                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "description": w.description},
+        "roofline": roofline,
+        "l2_to_sm_operand_bytes": {"analytic": plan.l2_to_sm_operand_bytes,
+                                   "analytic_unicast": uni_plan.l2_to_sm_operand_bytes,
+                                   "reduction_vs_unicast": uni_plan.l2_to_sm_operand_bytes /
+                                   max(1, plan.l2_to_sm_operand_bytes),
+                                   "measured": traffic_rec.get("lts_bytes") if traffic_rec else None},
+        "gpu_launches": launches,
+        "wall_s_timed_region": wall,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_through_host_api(g, p, args, device, stream, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, secs, rows, threads = oracle_rate(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K}"
+                                          f"{', first batch' if w.batch > 1 else ''}) in {secs:.1f} s"}
+    g.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_through_host_api(g, p: DeviceProblem, args, device, stream, dist):
+    """The same metric through gemm_run_host: pinned host inputs copied in and C copied out every step."""
+    import numpy as np
+    import torch
+    w = p.w
+    if w.batch > 1:
+        return {"value": None, "unit": "TFLOP/s", "note": "host-buffer entry point covers batch 1 only"}
+    A_h = torch.from_numpy(p.A_host.view(np.int16)).pin_memory()
+    B_h = torch.from_numpy(p.B_host.view(np.int16)).pin_memory()
+    esc = 4 if w.out == "f32" else 2
+    if p.C_host is not None:
+        C_h = torch.from_numpy(p.C_host.view(np.int16) if w.out == "bf16" else p.C_host.copy()).pin_memory()
+    else:
+        C_h = torch.empty(p.c_bytes // esc, dtype=torch.float32 if w.out == "f32" else torch.int16).pin_memory()
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        g.run_host(w.M, w.N, w.K, A_h, p.lda, B_h, p.ldb, C_h, p.ldc, w.alpha, w.beta, stream)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        g.run_host(w.M, w.N, w.K, A_h, p.lda, B_h, p.ldb, C_h, p.ldc, w.alpha, w.beta, stream)
+    local = time.perf_counter() - t0
+    elapsed, units = aggregate(dist, local, float(w.flops) * steps, device)
+    h2d = A_h.numel() * 2 + B_h.numel() * 2 + (C_h.numel() * esc if w.beta != 0.0 else 0)
+    return {"value": units / elapsed / 1e12, "unit": "TFLOP/s", "steps": steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(C_h.numel() * esc),
+            "ms_per_step": 1e3 * elapsed / steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return bench_reference(args, w)
+    return bench_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

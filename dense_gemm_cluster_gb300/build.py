@@ -19,9 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdensegemm.so")
-SOURCES = [os.path.join(CSRC, "gemm_host.cu")]
+SOURCES = [os.path.join(CSRC, "gemm_host.cu"), os.path.join(CSRC, "tma_bench.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "gemm_kernel.cuh"), os.path.join(CSRC, "ptx.cuh"),
-                     os.path.join(INCLUDE, "densegemm.h")]
+                     os.path.join(INCLUDE, "densegemm.h"), os.path.join(INCLUDE, "tma_bench.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

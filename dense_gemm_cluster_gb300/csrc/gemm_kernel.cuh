@@ -5,7 +5,10 @@
 // One CTA owns 128 rows of C (BLOCK_M). A cluster of cx * cy CTAs (cx along M,
 // cy along N) covers a "cluster tile" of cx*128 rows by cy*BN columns. Roles:
 //
-//   warp 0      producer: TMA loads of A/B k-blocks into an S-stage ring
+//   warp 0      A producer: TMA loads of A k-blocks into an S-stage ring
+//   warp 6      B producer: the same for B (two issuing threads keep the TMA
+//               engine fed: one thread's arm/issue/wait latency per k-block is
+//               longer than the tensor core's time for it)
 //   warp 1      TMEM allocation; MMA issue (one elected lane; with the pair MMA
 //               only the pair's even CTA issues)
 //   warps 2..5  epilogue: TMEM -> registers -> (alpha, beta) -> shared -> TMA store
@@ -47,7 +50,7 @@ namespace dgc {
 
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_K = 64;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF_BYTES = 4096;                              // 32 rows x 128 bytes
 constexpr int EPI_SMEM_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;    // double-buffered per warp
@@ -115,17 +118,26 @@ __device__ __noinline__ void report_timeout(const KernelParams& p, uint32_t code
 // Bounded wait on phase `parity` of the barrier at `bar`. Returns false (after
 // recording the reason unless another role already aborted) when the budget is
 // spent or the CTA is aborting.
+template <bool CLUSTER_SCOPE = false>
+__device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity) {
+    return CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+
+template <bool CLUSTER_SCOPE = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const KernelParams& p,
                                              volatile int* abort_flag, uint32_t code, uint32_t detail,
                                              long long tile) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
+    // The budget is counted in SM cycles (cheap to read) at 2 cycles per ns:
+    // at most twice the nominal time at the maximum clock, longer when slower.
+    const uint64_t c0 = clock_cycles();
+    const uint64_t budget = 2ull * p.timeout_ns;
     for (;;) {
 #pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 64; ++i)
+            if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > p.timeout_ns) {
+        if (clock_cycles() - c0 > budget) {
             report_timeout(p, code, detail, tile);
             *abort_flag = 1;
             return false;
@@ -148,40 +160,98 @@ __device__ __forceinline__ uint32_t col_mask(int rx, int ry, int cx) {
     return m;
 }
 
-// Loads this CTA's slice (index `slice` of `parts`) of one operand k-block.
-// K-major operand (rows x 64 K, 128-byte rows): slice by rows.
-// MN-major operand (64 K rows per 64-wide MN box): slice every box by K rows.
+// One operand's producer loop (run by one thread). Per k-block: wait until the
+// stage is released by every CTA this thread writes into, arm each receiver's
+// full barrier with the bytes of this thread's slice (through mapa for peers),
+// then issue the slice with one TMA load (K-major) or one per 64-wide box
+// (MN-major), multicast when the slice feeds several CTAs.
+//   K-major operand (rows x 64 K, 128-byte rows): slice = a band of rows.
+//   MN-major operand (64 K rows per 64-wide MN box): slice = a band of K rows of every box.
+struct OperandPlan {
+    const CUtensorMap* tmap;
+    uint32_t tile0;        // shared address of stage 0's tile
+    uint32_t tile_bytes;   // per stage
+    int rows;              // MN extent of the tile held by this CTA
+    int mn_major;
+    int slice, parts;      // this CTA's slice index and the group size
+    uint32_t mask;         // receivers (multicast) or just this CTA
+};
+
 template <int G>
-__device__ __forceinline__ void load_operand_slice(const CUtensorMap* tmap, uint32_t dst_tile,
-                                                   uint32_t bar, int mn_major, int rows, int mn0,
-                                                   int k0, int b, int slice, int parts, uint32_t mask) {
-    const bool mcast = parts > 1;
-    if (!mn_major) {
-        const int r = rows / parts;
-        const uint32_t dst = dst_tile + (uint32_t)(slice * r * 128);
-        const int y = mn0 + slice * r;
-        if (G == 1) {
-            if (mcast) tma_load_3d_mcast(dst, tmap, bar, k0, y, b, (uint16_t)mask);
-            else       tma_load_3d(dst, tmap, bar, k0, y, b);
-        } else {
-            if (mcast) tma_load_3d_pair_mcast(dst, tmap, bar, k0, y, b, (uint16_t)mask);
-            else       tma_load_3d_pair(dst, tmap, bar, k0, y, b);
-        }
-    } else {
-        const int kr = BLOCK_K / parts;
-        for (int box = 0; box < rows / 64; ++box) {
-            const uint32_t dst = dst_tile + (uint32_t)(box * BOX_BYTES + slice * kr * 128);
-            const int x = mn0 + box * 64;
-            const int y = k0 + slice * kr;
-            if (G == 1) {
-                if (mcast) tma_load_3d_mcast(dst, tmap, bar, x, y, b, (uint16_t)mask);
-                else       tma_load_3d(dst, tmap, bar, x, y, b);
-            } else {
-                if (mcast) tma_load_3d_pair_mcast(dst, tmap, bar, x, y, b, (uint16_t)mask);
-                else       tma_load_3d_pair(dst, tmap, bar, x, y, b);
+__device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan& op, bool is_a, uint32_t full0,
+                                        uint32_t empty0, uint32_t rank, uint32_t leader, int cx, int cy, int rx,
+                                        int ry, int BNv, int BN_CTAv, volatile int* abort_flag,
+                                        long long first_tile, long long tile_stride, int S) {
+    // Arm targets: the barrier that counts each receiver's bytes (the receiver
+    // itself, or its pair's even CTA), resolved once.
+    // Indexed by receiver rank with compile-time indices so it stays in registers.
+    uint32_t arm_addr[8];
+#pragma unroll
+    for (int d = 0; d < 8; ++d)
+        arm_addr[d] = (op.mask & (1u << d)) ? mapa(full0, G == 2 ? ((uint32_t)d & ~1u) : (uint32_t)d) : 0u;
+    const uint32_t slice_bytes = op.tile_bytes / (uint32_t)op.parts;
+    const uint32_t tma_bar0 = (G == 2) ? mapa(full0, leader) : full0;
+    const bool mcast = op.parts > 1;
+    const int kr = BLOCK_K / op.parts;           // MN-major: K rows per slice
+    const int rr = op.rows / op.parts;           // K-major: MN rows per slice
+    const uint32_t slice_off = op.mn_major ? (uint32_t)(op.slice * kr * 128) : (uint32_t)(op.slice * rr * 128);
+    bool extra_tx = is_a && (p.debug_flags & 1) != 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (long long t = first_tile; t < p.total_tiles; t += tile_stride) {
+        const TileCoord tc = tile_coord(p, t);
+        const int mn0 = is_a ? (tc.ctm * cx + rx) * BLOCK_M
+                             : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, p, abort_flag, ERR_WAIT_EMPTY, (uint32_t)stage, t))
+                return false;
+#pragma unroll
+            for (int d = 0; d < 8; ++d)
+                if (op.mask & (1u << d)) mbar_arrive_expect_tx_cluster(arm_addr[d] + 8u * stage, slice_bytes);
+            if (extra_tx) {
+                // Test hook: announce bytes that never come; the MMA's bounded
+                // wait on this stage must run out.
+                asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;"
+                             :: "r"(mapa(full0 + 8u * stage, leader)), "r"(16u) : "memory");
+                extra_tx = false;
             }
+            const uint32_t bar = tma_bar0 + 8u * stage;
+            const uint32_t dst = op.tile0 + stage * op.tile_bytes + slice_off;
+            const int k0 = kb * BLOCK_K;
+            if (!op.mn_major) {
+                const int y = mn0 + op.slice * rr;
+                if (G == 1) {
+                    if (mcast) tma_load_3d_mcast(dst, op.tmap, bar, k0, y, tc.b, (uint16_t)op.mask);
+                    else       tma_load_3d(dst, op.tmap, bar, k0, y, tc.b);
+                } else {
+                    if (mcast) tma_load_3d_pair_mcast(dst, op.tmap, bar, k0, y, tc.b, (uint16_t)op.mask);
+                    else       tma_load_3d_pair(dst, op.tmap, bar, k0, y, tc.b);
+                }
+            } else {
+                const int y = k0 + op.slice * kr;
+                for (int box = 0; box < op.rows / 64; ++box) {
+                    const uint32_t d = dst + (uint32_t)(box * BOX_BYTES);
+                    const int x = mn0 + box * 64;
+                    if (G == 1) {
+                        if (mcast) tma_load_3d_mcast(d, op.tmap, bar, x, y, tc.b, (uint16_t)op.mask);
+                        else       tma_load_3d(d, op.tmap, bar, x, y, tc.b);
+                    } else {
+                        if (mcast) tma_load_3d_pair_mcast(d, op.tmap, bar, x, y, tc.b, (uint16_t)op.mask);
+                        else       tma_load_3d_pair(d, op.tmap, bar, x, y, tc.b);
+                    }
+                }
+            }
+            if (++stage == S) { stage = 0; phase ^= 1u; }
         }
     }
+    // Drain: every stage this thread filled is released by all its receivers
+    // before the CTA may exit (no remote arrival may target an exited CTA).
+    for (int i = 0; i < S; ++i) {
+        if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, p, abort_flag, ERR_WAIT_EMPTY, (uint32_t)stage, -1))
+            return false;
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+    return true;
 }
 
 template <int BN, int G>
@@ -252,57 +322,20 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const long long first_tile = cluster_id_x();
     const long long tile_stride = num_clusters_x();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 6) {
+        // ------------------------------------------------------------ producers (A: warp 0, B: warp 6)
         if (lane == 0) {
-            prefetch_tmap(&tmA);
-            prefetch_tmap(&tmB);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            bool extra_tx = (p.debug_flags & 1) != 0;
-            const uint32_t sliceA = A_BYTES / gA;
-            const uint32_t sliceB = B_BYTES / gB;
-            for (long long t = first_tile; ok && t < p.total_tiles; t += tile_stride) {
-                const TileCoord tc = tile_coord(p, t);
-                const int m0 = (tc.ctm * cx + rx) * BLOCK_M;
-                const int nB0 = (tc.ctn * cy + ry) * BN + (G == 2 ? (rx & 1) * BN_CTA : 0);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag,
-                                      ERR_WAIT_EMPTY, (uint32_t)stage, t)) { ok = false; break; }
-                    const uint32_t full_local = smem_u32(&full_bar[stage]);
-                    // Arm every receiver's counting barrier before issuing.
-                    for (uint32_t m = maskA; m; m &= m - 1) {
-                        const uint32_t d = (uint32_t)(__ffs(m) - 1);
-                        mbar_arrive_expect_tx_cluster(mapa(full_local, G == 2 ? (d & ~1u) : d), sliceA);
-                    }
-                    for (uint32_t m = maskB; m; m &= m - 1) {
-                        const uint32_t d = (uint32_t)(__ffs(m) - 1);
-                        mbar_arrive_expect_tx_cluster(mapa(full_local, G == 2 ? (d & ~1u) : d), sliceB);
-                    }
-                    if (extra_tx) {
-                        // Test hook: announce bytes that never come; the MMA's
-                        // bounded wait on this stage must run out.
-                        asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;"
-                                     :: "r"(mapa(full_local, leader)), "r"(16u) : "memory");
-                        extra_tx = false;
-                    }
-                    const uint32_t tma_bar = (G == 2) ? mapa(full_local, leader) : full_local;
-                    const int k0 = kb * BLOCK_K;
-                    load_operand_slice<G>(&tmA, smem_u32(sA + stage * A_BYTES), tma_bar, p.a_mn_major,
-                                          BLOCK_M, m0, k0, tc.b, idxA, gA, maskA);
-                    load_operand_slice<G>(&tmB, smem_u32(sB + stage * B_BYTES), tma_bar, p.b_mn_major,
-                                          BN_CTA, nB0, k0, tc.b, idxB, gB, maskB);
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                }
+            const bool is_a = warp == 0;
+            OperandPlan op;
+            if (is_a) {
+                prefetch_tmap(&tmA);
+                op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, idxA, gA, maskA};
+            } else {
+                prefetch_tmap(&tmB);
+                op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, idxB, gB, maskB};
             }
-            // Drain: wait until every stage this CTA filled has been released by
-            // all of its receivers, so no remote arrival targets this CTA after exit.
-            for (int i = 0; ok && i < S; ++i) {
-                if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, p, abort_flag,
-                                  ERR_WAIT_EMPTY, (uint32_t)stage, -1)) break;
-                if (++stage == S) { stage = 0; phase ^= 1u; }
-            }
+            produce<G>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
+                       BN, BN_CTA, abort_flag, first_tile, tile_stride, S);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -318,8 +351,12 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                               (p.mcast_b ? col_mask<G>(px, ry, cx) : (1u << pr));
             }
             const bool local_only = (empty_mask == (1u << rank));
-            const uint32_t a_kstep = p.a_mn_major ? 16u * 128u : 32u;   // bytes per 16-element K step
-            const uint32_t b_kstep = p.b_mn_major ? 16u * 128u : 32u;
+            // Descriptors advance by adding (byte offset >> 4) to the start-address
+            // field (shared addresses stay below 256 KB, so the field cannot carry).
+            const uint32_t a_kstep = p.a_mn_major ? (16u * 128u) >> 4 : 32u >> 4;   // per 16-element K step
+            const uint32_t b_kstep = p.b_mn_major ? (16u * 128u) >> 4 : 32u >> 4;
+            const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA), p.a_mn_major != 0);
+            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sB), p.b_mn_major != 0);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t local_tile = 0;
@@ -327,22 +364,19 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (long long t = first_tile; ok && t < p.total_tiles; t += tile_stride, ++local_tile) {
                 const uint32_t acc = local_tile & 1u;
                 const uint32_t acc_phase = (local_tile >> 1) & 1u;
-                if (!wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p, abort_flag,
-                                  ERR_WAIT_TMEM_EMPTY, acc, t)) { ok = false; break; }
+                if (!wait_bounded<G == 2>(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p, abort_flag,
+                                          ERR_WAIT_TMEM_EMPTY, acc, t)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(smem_u32(&full_bar[stage]), phase, p, abort_flag,
                                       ERR_WAIT_FULL, (uint32_t)stage, t)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
-                    const uint32_t b_base = smem_u32(sB + stage * B_BYTES);
+                    const uint64_t a_st = adesc0 + ((stage * A_BYTES) >> 4);
+                    const uint64_t b_st = bdesc0 + ((stage * B_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < BLOCK_K / 16; ++k) {
-                        const uint64_t adesc = smem_desc_sw128(a_base + k * a_kstep, p.a_mn_major != 0);
-                        const uint64_t bdesc = smem_desc_sw128(b_base + k * b_kstep, p.b_mn_major != 0);
-                        mma_bf16<G>(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < BLOCK_K / 16; ++k)
+                        mma_bf16<G>(d_tmem, a_st + k * a_kstep, b_st + k * b_kstep, idesc, (kb | k) != 0 ? 1u : 0u);
                     const uint32_t eb = smem_u32(&empty_bar[stage]);
                     if (local_only) mma_commit<G>(eb);
                     else            mma_commit_mcast<G>(eb, (uint16_t)empty_mask);
@@ -367,8 +401,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint8_t* stage_ptr = sEpi + ew * 2 * EPI_BUF_BYTES;
         const int CW = p.out_f32 ? 32 : 64;               // columns per 128-byte store row
         const int chunks = BN / CW;
-        const uint32_t tempty_target = (G == 2) ? mapa(smem_u32(&tempty_bar[0]), leader)
-                                                : smem_u32(&tempty_bar[0]);
+
         const bool use_beta = p.beta != 0.0f;
         uint32_t local_tile = 0;
         uint32_t buf = 0;
@@ -404,7 +437,10 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     // All of this accumulator is in registers: hand it back.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(tempty_target + acc * 8u);
+                    if (lane == 0) {
+                        if (G == 2) mbar_arrive_cluster(mapa(smem_u32(&tempty_bar[acc]), leader));
+                        else        mbar_arrive_local(smem_u32(&tempty_bar[acc]));
+                    }
                 }
                 // alpha * acc + beta * C_in, in fp32.
                 if (use_beta) {

@@ -222,3 +222,43 @@ class Gemm:
             self.close()
         except Exception:
             pass
+
+
+# ---------------------------------------------------------------- TMA microbenchmark (include/tma_bench.h)
+TMA_BENCH_UNICAST = 0
+TMA_BENCH_MULTICAST = 1
+TMA_BENCH_MULTICAST_SLICED = 2
+
+
+class tma_bench_options_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "mode", "cluster", "ctas", "box_rows", "stages", "iters", "warmup", "streaming_stride")] + [
+        ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+_lib.tma_bench_run.argtypes = [ctypes.POINTER(tma_bench_options_t), _vp, _i64, _i64, _i64, _vp, _vp, _vp,
+                               ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_double),
+                               ctypes.POINTER(ctypes.c_double), _vp]
+_lib.tma_bench_run.restype = _i32
+_lib.tma_bench_query_status.argtypes = [_vp]
+_lib.tma_bench_query_status.restype = _i32
+_lib.tma_bench_last_error.argtypes = []
+_lib.tma_bench_last_error.restype = ctypes.c_char_p
+
+
+def tma_bench_run(opt: tma_bench_options_t, src, rows, cols, ld, cycles, ns, verify, stream=None):
+    """Returns (status, ctas_used, delivered_bytes, issued_bytes)."""
+    n = _i32(0)
+    d = ctypes.c_double(0.0)
+    i = ctypes.c_double(0.0)
+    s = _lib.tma_bench_run(ctypes.byref(opt), _ptr(src), rows, cols, ld, _ptr(cycles), _ptr(ns), _ptr(verify),
+                           ctypes.byref(n), ctypes.byref(d), ctypes.byref(i), _stream(stream))
+    return s, n.value, d.value, i.value
+
+
+def tma_bench_query_status(stream=None) -> int:
+    return _lib.tma_bench_query_status(_stream(stream))
+
+
+def tma_bench_last_error() -> str:
+    return (_lib.tma_bench_last_error() or b"").decode()

@@ -1,0 +1,82 @@
+"""The synthetic workloads the library is measured and checked on.
+
+Each entry names a GEMM (or the batched score form) with its sizes, input
+distributions, layouts and the operand-sharing mode it runs in. Inputs come
+from ``inputs`` with seed 0 (A / Q on stream 0, B / K on stream 1, C_in on
+stream 2). Layouts the workload text leaves open are row-major.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    batch: int = 1
+    dist: str = "normal"            # "normal" (N(0,1)) or "uniform" (U(-1,1))
+    scale: float = 1.0              # multiplies A and B draws before rounding
+    layout_a: str = "row"
+    layout_b: str = "row"
+    layout_c: str = "row"
+    out: str = "bf16"
+    alpha: float = 1.0
+    beta: float = 0.0
+    c_dist: str = "normal"
+    options: dict = field(default_factory=dict)
+    description: str = ""
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K * self.batch
+
+    def min_hbm_bytes(self) -> int:
+        """Each input read once, C written once (and read once when beta != 0)."""
+        esc = 4 if self.out == "f32" else 2
+        b = (self.M * self.K + self.K * self.N) * 2 * self.batch + self.M * self.N * esc * self.batch
+        if self.beta != 0.0:
+            b += self.M * self.N * esc * self.batch
+        return b
+
+
+WORKLOADS = {
+    "gemm256_f32_mcastB": Workload(
+        "gemm256_f32_mcastB", 256, 256, 256, dist="normal", out="f32",
+        options=dict(mode="mcast", mcast_b=1, cluster_m=2, cluster_n=1),
+        description="GEMM 256^3, N(0,1), fp32 out, row-major, 2-CTA cluster multicasting B"),
+    "gemm4096_bf16_cluster2x1": Workload(
+        "gemm4096_bf16_cluster2x1", 4096, 4096, 4096, dist="uniform", layout_a="row", layout_b="col",
+        options=dict(mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=1),
+        description="GEMM 4096^3, U(-1,1), A row-major, B column-major, bf16 out, 2x1 cluster "
+                    "multicasting A and B (A's multicast extent is 1)"),
+    "gemm4096_bf16_cluster2x2": Workload(
+        "gemm4096_bf16_cluster2x2", 4096, 4096, 4096, dist="uniform", layout_a="row", layout_b="col",
+        options=dict(mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2),
+        description="GEMM 4096^3 as above with a 2x2 cluster multicasting both A and B"),
+    "gemm8192_bf16_pair_mcastB4": Workload(
+        "gemm8192_bf16_pair_mcastB4", 8192, 8192, 8192, dist="normal", scale=1.0 / math.sqrt(8192),
+        out="bf16", beta=0.5,
+        options=dict(mode="mcast", mcast_b=1, cluster_m=4, cluster_n=1, cta_group=2, block_n=256),
+        description="GEMM 8192^3, N(0,1)/sqrt(K), bf16 out, beta=0.5 with bf16 C ~ N(0,1), "
+                    "cta_group::2 256x256 tiles, 4-CTA cluster multicasting B"),
+    "scores_8x16x4096x4096x128": Workload(
+        "scores_8x16x4096x4096x128", 4096, 4096, 128, batch=128, dist="normal", layout_a="row",
+        layout_b="col", out="f32",
+        options=dict(mode="mcast", mcast_b=1, cluster_m=2, cluster_n=1),
+        description="attention scores S = Q K^T, batch 8 x heads 16, seq 4096, head dim 128, "
+                    "N(0,1) bf16 Q/K, fp32 S, K tile multicast across the Q-tile CTAs"),
+    "skinny_16384x128x8192": Workload(
+        "skinny_16384x128x8192", 16384, 128, 8192, dist="uniform",
+        options=dict(mode="mcast", mcast_b=1, cluster_m=4, cluster_n=1, block_n=128),
+        description="skinny GEMM M=16384, N=128, K=8192, U(-1,1), bf16 out, small B multicast along M"),
+    "skinny_128x16384x8192": Workload(
+        "skinny_128x16384x8192", 128, 16384, 8192, dist="uniform",
+        options=dict(mode="mcast", mcast_a=1, cluster_m=1, cluster_n=4, block_n=128),
+        description="skinny GEMM M=128, N=16384, K=8192, U(-1,1), bf16 out, small A multicast along N"),
+}
+
+DEFAULT = "gemm4096_bf16_cluster2x1"

@@ -85,7 +85,8 @@ typedef struct {
     int stages;         /* shared-memory pipeline depth; 0 = as many as fit */
     int max_clusters;   /* cap on the persistent grid, in clusters; 0 = as many as are co-resident */
     int group_m;        /* raster band height, in cluster tiles along M; 0 = 8 */
-    uint64_t wait_timeout_ns; /* bound on every in-kernel wait; 0 = 2 s */
+    uint64_t wait_timeout_ns; /* bound on every in-kernel wait, counted as 2 SM cycles per ns
+                                 (this long at 2 GHz, longer at lower clocks); 0 = 2 s */
     int debug_flags;    /* 0, or GEMM_DEBUG_EXTRA_TX (tests only) */
 } gemm_options_t;
 

@@ -25,7 +25,7 @@ def declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"\b(gemm_\w+)\s*\(", text))
+            names |= set(re.findall(r"\b((?:gemm|tma_bench)_\w+)\s*\(", text))
     return sorted(names)
 
 

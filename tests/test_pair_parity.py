@@ -1,0 +1,67 @@
+"""GPU parity of the 2-SM pair MMA (tcgen05 cta_group::2), alone and with cluster multicast.
+
+"Clusters, distributed shared memory & cluster launch control", section "Two
+CTAs, one MMA -- cta_group::2": A is split by rows across the pair, B by
+columns, each CTA keeps its half of the 256-row accumulator; the product is
+the same GEMM, so the oracle is unchanged.
+"""
+import numpy as np
+import pytest
+
+from gpu_cases import Problem, assert_close, options_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def G():
+    import torch
+    from dense_gemm_cluster_gb300 import gemm
+    assert torch.cuda.is_available()
+    return gemm
+
+
+def _run(G, p, alpha=1.0, beta=0.0, **opts):
+    g = G.Gemm(0, **options_for(p, **opts))
+    try:
+        dC = p.run(g, alpha, beta)
+        assert g.query_status() == G.GEMM_OK, G.gemm_last_error(g.handle)
+        return p.result(dC)
+    finally:
+        g.close()
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("la,lb", [("row", "col"), ("row", "row"), ("col", "row")])
+def test_pair_unicast(G, bn, la, lb):
+    p = Problem(512, 768, 384, la=la, lb=lb, out="bf16", seed=11)
+    got = _run(G, p, cta_group=2, cluster_m=2, block_n=bn)
+    assert_close(got, p.reference(), 384, "bf16", f"pair bn={bn} {la}/{lb}")
+
+
+@pytest.mark.parametrize("cm,cn,ma,mb", [(4, 1, 0, 1), (2, 2, 1, 0), (4, 2, 1, 1), (2, 4, 1, 0), (8, 1, 0, 1)])
+def test_pair_with_multicast_bitwise_equals_pair_unicast(G, cm, cn, ma, mb):
+    p = Problem(1100, 1300, 512, la="row", lb="row", out="bf16", seed=12)
+    base = _run(G, p, cta_group=2, cluster_m=2, cluster_n=1)
+    got = _run(G, p, cta_group=2, cluster_m=cm, cluster_n=cn, mode="mcast", mcast_a=ma, mcast_b=mb)
+    assert_close(got, p.reference(), 512, "bf16", f"pair cluster {cm}x{cn} A{ma} B{mb}")
+    assert np.array_equal(got, base)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (129, 257, 65), (383, 130, 300), (256, 1, 17)])
+def test_pair_ragged(G, M, N, K):
+    p = Problem(M, N, K, la="row", lb="row", out="f32", seed=13)
+    got = _run(G, p, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1)
+    assert_close(got, p.reference(), K, "f32", f"pair ragged {M}x{N}x{K}")
+
+
+def test_pair_beta_and_column_major_c(G):
+    p = Problem(640, 520, 256, la="row", lb="row", lc="col", out="bf16", beta=0.5, seed=14)
+    got = _run(G, p, 1.0, 0.5, cta_group=2, cluster_m=1, cluster_n=2)   # C^T: cluster_n becomes the pair axis
+    assert_close(got, p.reference(1.0, 0.5), 256, "bf16", "pair beta col-major C")
+
+
+def test_pair_persistent_few_clusters(G):
+    p = Problem(1536, 1024, 512, seed=15)
+    got = _run(G, p, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1, max_clusters=2, stages=3)
+    assert_close(got, p.reference(), 512, "bf16", "pair persistent")
