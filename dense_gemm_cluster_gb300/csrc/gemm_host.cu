@@ -569,3 +569,122 @@ extern "C" gemm_status_t gemm_query_status(gemm_handle_t h, void* stream_v) {
     cudaMemset(h->d_status, 0, 16);
     return GEMM_ERR_DEVICE_TIMEOUT;
 }
+
+// ---------------------------------------------------------------------------
+// gemm_run_noalloc: gemm_run without a handle and without any device
+// allocation. The kernel's status record (16 bytes) lives in this file-scope
+// static array instead of handle-owned memory. In host code the array's name is
+// only a stand-in for the symbol; its device address comes from
+// cudaGetSymbolAddress, taken once per device with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[256];
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = sizeof(g_noalloc_scratch);
+constexpr size_t kStatusRecordBytes = 16;
+constexpr int kMaxDevices = 64;
+
+struct NoAllocDevice {
+    bool ready = false;
+    void* scratch = nullptr;         // device address of g_noalloc_scratch on this device
+    int sm_count = 0;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    bool smem_set[2][2] = {{false, false}, {false, false}};
+    int occ[2][2][9] = {};
+};
+
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// One-time set-up on `device`; the caller holds g_noalloc_mutex.
+gemm_status_t noalloc_setup(int device) {
+    NoAllocDevice& d = g_noalloc_dev[device];
+    if (d.ready) return GEMM_OK;
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess)
+        return fail(nullptr, GEMM_ERR_CUDA, "cudaGetDeviceProperties(%d): %s", device, cudaGetErrorString(e));
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(nullptr, GEMM_ERR_NOT_SM103, "device %d is sm_%d%d; this library is built for sm_103a",
+                    device, prop.major, prop.minor);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != device) cudaSetDevice(device);
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (prev != device) cudaSetDevice(prev);
+    if (e != cudaSuccess || !ptr)
+        return fail(nullptr, GEMM_ERR_CUDA, "cudaGetSymbolAddress(static status record): %s", cudaGetErrorString(e));
+    if (e2 != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(nullptr, GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    d.scratch = ptr;
+    d.sm_count = prop.multiProcessorCount;
+    d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    d.ready = true;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_noalloc(const gemm_options_t* opt, int device, int64_t M, int64_t N, int64_t K,
+                                          const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                                          int64_t ldc, float alpha, float beta, void* stream,
+                                          uint32_t* status_out) {
+    if (!opt) return fail(nullptr, GEMM_ERR_INVALID_ARG, "gemm_run_noalloc needs options");
+    if (device < 0 || device >= kMaxDevices) return fail(nullptr, GEMM_ERR_INVALID_ARG, "bad device %d", device);
+    if (kStatusRecordBytes > kNoAllocScratchBytes)
+        return fail(nullptr, GEMM_ERR_UNSUPPORTED, "a launch needs %zu bytes of static scratch; the array holds %zu",
+                    kStatusRecordBytes, kNoAllocScratchBytes);
+    if (opt->mode == GEMM_MODE_MCAST && (opt->mcast_a || opt->mcast_b) && world_is_multi_gpu())
+        return fail(nullptr, GEMM_ERR_UNSUPPORTED,
+                    "cluster multicast is single-GPU only; WORLD_SIZE > 1 requires unicast or the pair MMA");
+    // A handle on the host stack that points at the static record: no device memory is allocated.
+    gemm_handle_s local;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        gemm_status_t s = noalloc_setup(device);
+        if (s != GEMM_OK) return s;
+        const NoAllocDevice& d = g_noalloc_dev[device];
+        local.opt = *opt;
+        if (local.opt.wait_timeout_ns == 0) local.opt.wait_timeout_ns = kDefaultTimeoutNs;
+        local.device = device;
+        local.sm_count = d.sm_count;
+        local.d_status = static_cast<unsigned int*>(d.scratch);
+        local.encode = d.encode;
+        memcpy(local.smem_set, d.smem_set, sizeof local.smem_set);
+        memcpy(local.occ_key, d.occ, sizeof local.occ_key);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != device) cudaSetDevice(device);
+    // The record must start at zero: earlier calls leave their contents behind.
+    cudaError_t e = cudaMemsetAsync(local.d_status, 0, kStatusRecordBytes, st);
+    if (prev != device) cudaSetDevice(prev);
+    if (e != cudaSuccess) return fail(nullptr, GEMM_ERR_CUDA, "clearing the status record: %s", cudaGetErrorString(e));
+    gemm_status_t s = run_impl(&local, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, alpha, beta, stream);
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        NoAllocDevice& d = g_noalloc_dev[device];
+        memcpy(d.smem_set, local.smem_set, sizeof d.smem_set);
+        memcpy(d.occ, local.occ_key, sizeof d.occ);
+    }
+    if (s != GEMM_OK) {
+        g_thread_error = local.err;
+        return s;
+    }
+    if (status_out) {
+        if (prev != device) cudaSetDevice(device);
+        e = cudaMemcpyAsync(status_out, local.d_status, kStatusRecordBytes, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (prev != device) cudaSetDevice(prev);
+        if (e != cudaSuccess) return fail(nullptr, GEMM_ERR_CUDA, "reading the status record: %s", cudaGetErrorString(e));
+        if (status_out[0] != 0)
+            return fail(nullptr, GEMM_ERR_DEVICE_TIMEOUT, "bounded wait expired (code %u, stage/buffer %u, CTA %u)",
+                        status_out[0], status_out[1], status_out[2]);
+    }
+    return GEMM_OK;
+}

@@ -79,6 +79,9 @@ _lib.gemm_launch_count.argtypes = [_vp]
 _lib.gemm_launch_count.restype = _i64
 _lib.gemm_destroy.argtypes = [_vp]
 _lib.gemm_destroy.restype = _i32
+_lib.gemm_run_noalloc.argtypes = [_OPT_P, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp,
+                                  ctypes.POINTER(ctypes.c_uint32)]
+_lib.gemm_run_noalloc.restype = _i32
 
 
 def library_path() -> str:
@@ -159,6 +162,14 @@ def gemm_launch_count(h) -> int:
 
 def gemm_destroy(h) -> int:
     return _lib.gemm_destroy(h)
+
+
+def gemm_run_noalloc(opt: gemm_options_t, device, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream=None,
+                     status_out=None) -> int:
+    """The allocation-free variant of gemm_run (no handle). ``status_out``: None, or a
+    ``(ctypes.c_uint32 * 4)`` array that receives the status record (the call then synchronizes)."""
+    return _lib.gemm_run_noalloc(ctypes.byref(opt), device, M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                 alpha, beta, _stream(stream), status_out)
 
 
 # ---------------------------------------------------------------- convenience

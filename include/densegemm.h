@@ -169,6 +169,33 @@ const char *gemm_last_error(gemm_handle_t h);
 /* Number of GEMM kernel launches this handle has made (for launch accounting). */
 int64_t gemm_launch_count(gemm_handle_t h);
 
+/* gemm_run for callers that cannot allocate device memory. (The pages describe no
+ * such entry point; it exists for users of this library.) Some callers must not
+ * call cudaMalloc: code running while a memory pool has already reserved the
+ * device's memory, allocator callbacks, plugins whose host forbids allocation,
+ * or latency-critical paths that cannot afford cudaMalloc's implicit device
+ * synchronization. gemm_create allocates a device status record; this call needs
+ * no handle and allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine). Its status record lives in a 256-byte static device array that the
+ * library holds on every GPU that loads it until the process exits; a launch
+ * uses 16 bytes of it, and a launch needing more than the array holds is
+ * rejected with GEMM_ERR_UNSUPPORTED.
+ *   - Same arguments and semantics as gemm_create + gemm_run, with the options
+ *     and the device given directly; the caller passes A, B and C (device memory).
+ *   - The first call on each device does a one-time set-up with that device
+ *     current (it looks up the array's device address and the driver's
+ *     tensor-map encoder); make that first call before any stream capture.
+ *   - Every call shares the one array and clears the status record on `stream`
+ *     before its launch. Calls whose kernels overlap on the GPU race on it, so
+ *     a timeout seen by one may be reported to another.
+ *   - status_out: NULL for a fully asynchronous call; otherwise a host array of
+ *     4 uint32 that receives the status record after the call synchronizes
+ *     `stream` (GEMM_ERR_DEVICE_TIMEOUT if a bounded wait expired). */
+gemm_status_t gemm_run_noalloc(const gemm_options_t *opt, int device, int64_t M, int64_t N, int64_t K,
+                               const void *A, int64_t lda, const void *B, int64_t ldb,
+                               void *C, int64_t ldc, float alpha, float beta, void *stream,
+                               uint32_t *status_out);
+
 /* Frees the handle and everything it owns. Safe on NULL. */
 gemm_status_t gemm_destroy(gemm_handle_t h);
 
