@@ -358,15 +358,26 @@ def bench_ours(args, w: Workload):
     ms_per_step = 1e3 * elapsed / args.steps
 
     peaks, peaks_kind = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     avg_launch_s = local_s / args.steps
-    achieved = w.flops / avg_launch_s / 1e12
     traffic_rec = recorded_traffic(w.name)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic_rec["dram_bytes"] if traffic_rec else None,
-                "peak_source": f"bf16_tflops (burst) of {peaks_kind}",
-                "algorithmic_flops_per_launch": w.flops,
-                "hbm_gbs_at_min_bytes": w.min_hbm_bytes() / avg_launch_s / 1e9}
+    intensity = w.flops / w.min_hbm_bytes()
+    ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)
+    if intensity >= ridge:
+        achieved = w.flops / avg_launch_s / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tensor_peak, "peak_source": f"bf16_tflops (burst) of {peaks_kind}",
+                    "algorithmic_flops_per_launch": w.flops}
+    else:
+        achieved = w.min_hbm_bytes() / avg_launch_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "peak_source": f"hbm_gbs (copy) of {peaks_kind}",
+                    "algorithmic_bytes_per_launch": w.min_hbm_bytes()}
+    roofline.update({"traffic": traffic_rec["dram_bytes"] if traffic_rec else None,
+                     "arithmetic_intensity": intensity, "ridge": ridge,
+                     "tflops": w.flops / avg_launch_s / 1e12,
+                     "hbm_gbs_at_min_bytes": w.min_hbm_bytes() / avg_launch_s / 1e9})
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
