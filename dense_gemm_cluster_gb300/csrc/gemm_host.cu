@@ -69,6 +69,8 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
                     o.cluster_m, o.cluster_n);
     if (o.block_n != 0 && o.block_n != 128 && o.block_n != 256)
         return fail(err, GEMM_ERR_UNSUPPORTED, "block_n must be 0, 128 or 256");
+    if (o.block_k != 0 && o.block_k != 64 && o.block_k != 128)
+        return fail(err, GEMM_ERR_UNSUPPORTED, "block_k must be 0, 64 or 128");
     if (o.group_m < 0 || o.max_clusters < 0 || o.stages < 0)
         return fail(err, GEMM_ERR_INVALID_ARG, "group_m, max_clusters and stages must be >= 0");
     if (M < 0 || N < 0 || K < 0 || batch < 0)
@@ -92,12 +94,24 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     if (gB == 1) mb = 0;
 
     const int BN = o.block_n ? o.block_n : 256;
-    const int a_bytes = dgc::BLOCK_M * dgc::BLOCK_K * 2;
-    const int b_bytes = (BN / G) * dgc::BLOCK_K * 2;
-    const int stage_bytes = a_bytes + b_bytes;
     // 1024 for aligning the dynamic base, the epilogue staging, then per stage a
     // full and an empty barrier, plus 5 barriers, the TMEM address and the abort flag.
     const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 5 * 8 + 16;
+    auto stage_bytes_for = [&](int bk) { return dgc::BLOCK_M * bk * 2 + (BN / G) * bk * 2; };
+    // Operands as launched (after the C^T transpose): K-major ones need K % 64 == 0
+    // for the k-split map that 128-wide stages use.
+    const bool a_kmajor = (swap ? o.layout_b == GEMM_COL_MAJOR : o.layout_a == GEMM_ROW_MAJOR);
+    const bool b_kmajor = (swap ? o.layout_a == GEMM_ROW_MAJOR : o.layout_b == GEMM_COL_MAJOR);
+    const bool k_split_ok = (K % dgc::ATOM_K) == 0 || (!a_kmajor && !b_kmajor);
+    int BK = o.block_k;
+    if (BK == 0) {
+        // 128-wide stages halve the producers' per-byte issue cost; keep them when
+        // at least three still fit in shared memory.
+        BK = (k_split_ok && (kMaxSmemPerCta - fixed) / (stage_bytes_for(128) + 16) >= 3) ? 128 : 64;
+    }
+    if (BK == 128 && !k_split_ok)
+        return fail(err, GEMM_ERR_UNSUPPORTED, "block_k 128 needs K a multiple of 64 when an operand is K-major");
+    const int stage_bytes = stage_bytes_for(BK);
     int S = o.stages;
     const int max_s = (kMaxSmemPerCta - fixed) / (stage_bytes + 16);
     if (S == 0) S = max_s < 8 ? max_s : 8;
@@ -120,7 +134,7 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     memset(&p, 0, sizeof p);
     p.block_m = dgc::BLOCK_M;
     p.block_n = BN;
-    p.block_k = dgc::BLOCK_K;
+    p.block_k = BK;
     p.stages = S;
     p.smem_bytes = fixed + S * (stage_bytes + 16);
     p.cluster_m = cm;
@@ -136,19 +150,24 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     if (o.max_clusters > 0 && o.max_clusters < clusters) clusters = o.max_clusters;
     if (p.tiles < clusters) clusters = p.tiles;
     p.clusters = clusters;
-    const int64_t k_pad = ceil_div(K, dgc::BLOCK_K) * dgc::BLOCK_K;
+    const int64_t k_pad = ceil_div(K, BK) * BK;
     p.l2_to_sm_operand_bytes = p.tiles * cm * cn * k_pad * 2 * (dgc::BLOCK_M / gA + (BN / G) / gB);
     return GEMM_OK;
 }
 
-template <int BN, int G>
+template <int BN, int G, int BK>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&dgc::dgc_gemm_kernel<BN, G>);
+    return reinterpret_cast<void*>(&dgc::dgc_gemm_kernel<BN, G, BK>);
 }
 
-void* pick_kernel(int BN, int G) {
-    if (BN == 256) return G == 1 ? kernel_ptr<256, 1>() : kernel_ptr<256, 2>();
-    return G == 1 ? kernel_ptr<128, 1>() : kernel_ptr<128, 2>();
+template <int BK>
+void* pick_kernel_bk(int BN, int G) {
+    if (BN == 256) return G == 1 ? kernel_ptr<256, 1, BK>() : kernel_ptr<256, 2, BK>();
+    return G == 1 ? kernel_ptr<128, 1, BK>() : kernel_ptr<128, 2, BK>();
+}
+
+void* pick_kernel(int BN, int G, int BK) {
+    return BK == 128 ? pick_kernel_bk<128>(BN, G) : pick_kernel_bk<64>(BN, G);
 }
 
 // K == 0: C <- beta * C (zero when beta == 0, without reading C).
@@ -183,8 +202,8 @@ struct gemm_handle_s {
     void* stage_ptr[3] = {nullptr, nullptr, nullptr};
     size_t stage_cap[3] = {0, 0, 0};
     int64_t launches = 0;
-    bool smem_set[2][2] = {{false, false}, {false, false}};
-    int occ_key[2][2][9];       // cached max active clusters per (BN, G, cluster size)
+    bool smem_set[2][2][2] = {};
+    int occ_key[2][2][2][9];    // cached max active clusters per (BN, G, BK, cluster size)
 };
 
 static const char* kStatusNames[] = {
@@ -312,6 +331,40 @@ static gemm_status_t encode_map(gemm_handle_s* h, CUtensorMap* map, CUtensorMapD
     return GEMM_OK;
 }
 
+// Encodes the k-split view of a K-major bf16 operand (K a multiple of 64):
+// dims {64 K, rows, K/64, batch} with the 64-element atoms 128 bytes apart, so one
+// box {64, box_rows, box_atoms, 1} lands as box_atoms consecutive swizzled tiles.
+static gemm_status_t encode_ksplit(gemm_handle_s* h, CUtensorMap* map, const void* ptr, int64_t K, int64_t rows,
+                                   int64_t batch, int64_t ld, int64_t stride, uint32_t box_rows, uint32_t box_atoms,
+                                   const char* what) {
+    cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64), (cuuint64_t)batch};
+    int64_t bstride = batch > 1 ? stride : ((ld * rows + 15) / 16) * 16;
+    if (bstride <= 0) bstride = 16;
+    cuuint64_t strides[3] = {(cuuint64_t)(ld * 2), 128, (cuuint64_t)(bstride * 2)};
+    cuuint32_t box[4] = {64, box_rows, box_atoms, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult res = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS)
+        return fail(&h->err, GEMM_ERR_INVALID_ARG,
+                    "cuTensorMapEncodeTiled(%s, k-split) failed with %d (K %lld, rows %lld, batch %lld, ld %lld)",
+                    what, (int)res, (long long)K, (long long)rows, (long long)batch, (long long)ld);
+    return GEMM_OK;
+}
+
+// Box of one issuer's slice of a K-major tile of `rows` rows and `atoms` atoms
+// shared by `parts` issuers: whole atoms first, then bands of rows.
+static void ksplit_box(int rows, int atoms, int parts, uint32_t& box_rows, uint32_t& box_atoms) {
+    if (parts <= atoms) {
+        box_rows = (uint32_t)rows;
+        box_atoms = (uint32_t)(atoms / parts);
+    } else {
+        box_rows = (uint32_t)(rows / (parts / atoms));
+        box_atoms = 1;
+    }
+}
+
 static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                               int64_t strideA, const void* B, int64_t ldb, int64_t strideB, void* C,
                               int64_t ldc, int64_t strideC, int64_t batch, float alpha, float beta,
@@ -390,20 +443,32 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     const int BN = pl.block_n, G = pl.cta_group;
     const int gA = pl.group_a, gB = pl.group_b;
 
+    const int BK = pl.block_k;
+    const int atoms = BK / dgc::ATOM_K;
+    const bool kmap4 = (r.K % dgc::ATOM_K) == 0;
     CUtensorMap tmA, tmB, tmC;
-    if (!opA.mn_major)
+    uint32_t br, ba;
+    if (!opA.mn_major && kmap4) {
+        ksplit_box(dgc::BLOCK_M, atoms, gA, br, ba);
+        s = encode_ksplit(h, &tmA, opA.ptr, r.K, r.M, batch, opA.ld, opA.stride, br, ba, "A");
+    } else if (!opA.mn_major) {
         s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.K, r.M, batch, opA.ld, opA.stride,
                        64, dgc::BLOCK_M / gA, "A");
-    else
+    } else {
         s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.M, r.K, batch, opA.ld, opA.stride,
-                       64, dgc::BLOCK_K / gA, "A");
+                       64, BK / gA, "A");
+    }
     if (s != GEMM_OK) return s;
-    if (!opB.mn_major)
+    if (!opB.mn_major && kmap4) {
+        ksplit_box(BN / G, atoms, gB, br, ba);
+        s = encode_ksplit(h, &tmB, opB.ptr, r.K, r.N, batch, opB.ld, opB.stride, br, ba, "B");
+    } else if (!opB.mn_major) {
         s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.K, r.N, batch, opB.ld, opB.stride,
                        64, (BN / G) / gB, "B");
-    else
+    } else {
         s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.N, r.K, batch, opB.ld, opB.stride,
-                       64, dgc::BLOCK_K / gB, "B");
+                       64, BK / gB, "B");
+    }
     if (s != GEMM_OK) return s;
     s = encode_map(h, &tmC, r.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, esc,
                    C, r.N, r.M, batch, ldc, strideC, r.out_f32 ? 32 : 64, 32, "C");
@@ -415,7 +480,9 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     kp.N = (int)r.N;
     kp.K = (int)r.K;
     kp.batch = (int)batch;
-    kp.num_kb = (int)ceil_div(r.K, dgc::BLOCK_K);
+    kp.num_kb = (int)ceil_div(r.K, BK);
+    kp.a_kmap4 = !opA.mn_major && kmap4;
+    kp.b_kmap4 = !opB.mn_major && kmap4;
     kp.cx = pl.cluster_m;
     kp.cy = pl.cluster_n;
     kp.mcast_a = r.mcast_a;
@@ -437,12 +504,12 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     kp.status = h->d_status;
     kp.timeout_ns = o.wait_timeout_ns;
 
-    void* fn = pick_kernel(BN, G);
-    const int bi = BN == 256 ? 1 : 0, gi = G - 1;
-    if (!h->smem_set[bi][gi]) {
+    void* fn = pick_kernel(BN, G, BK);
+    const int bi = BN == 256 ? 1 : 0, gi = G - 1, ki = BK == 128 ? 1 : 0;
+    if (!h->smem_set[bi][gi][ki]) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerCta);
         if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
-        h->smem_set[bi][gi] = true;
+        h->smem_set[bi][gi][ki] = true;
     }
     const int cs = pl.cluster_m * pl.cluster_n;
     cudaLaunchConfig_t cfg;
@@ -457,7 +524,7 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int& occ = h->occ_key[bi][gi][cs];
+    int& occ = h->occ_key[bi][gi][ki][cs];
     if (occ == 0) {
         cfg.gridDim = dim3((unsigned)(cs * (h->sm_count / cs)), 1, 1);
         int n = 0;
@@ -589,8 +656,8 @@ struct NoAllocDevice {
     void* scratch = nullptr;         // device address of g_noalloc_scratch on this device
     int sm_count = 0;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    bool smem_set[2][2] = {{false, false}, {false, false}};
-    int occ[2][2][9] = {};
+    bool smem_set[2][2][2] = {};
+    int occ[2][2][2][9] = {};
 };
 
 NoAllocDevice g_noalloc_dev[kMaxDevices];

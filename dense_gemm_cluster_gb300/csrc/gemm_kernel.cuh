@@ -49,12 +49,11 @@
 namespace dgc {
 
 constexpr int BLOCK_M = 128;
-constexpr int BLOCK_K = 64;
+constexpr int ATOM_K = 64;                                       // bf16 elements per 128-byte swizzle row
 constexpr int NUM_THREADS = 224;
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_BUF_BYTES = 4096;                              // 32 rows x 128 bytes
 constexpr int EPI_SMEM_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;    // double-buffered per warp
-constexpr int BOX_BYTES = 8192;                                  // 64 rows x 128 bytes
 
 // Error codes written to status[0] by a wait that ran out.
 enum : uint32_t {
@@ -69,7 +68,8 @@ enum : uint32_t {
 struct KernelParams {
     int M, N, K;             // problem (after any transpose for column-major C)
     int batch;
-    int num_kb;              // ceil(K / 64), >= 1
+    int num_kb;              // ceil(K / BK), >= 1
+    int a_kmap4, b_kmap4;    // K-major operand described by the 4-D k-split map {64, rows, K/64, batch}
     int cx, cy;              // cluster extent along M / N (CTAs)
     int mcast_a, mcast_b;
     int a_mn_major, b_mn_major;
@@ -160,31 +160,60 @@ __device__ __forceinline__ uint32_t col_mask(int rx, int ry, int cx) {
     return m;
 }
 
-// One operand's producer loop (run by one thread). Per k-block: wait until the
-// stage is released by every CTA this thread writes into, arm each receiver's
-// full barrier with the bytes of this thread's slice (through mapa for peers),
-// then issue the slice with one TMA load (K-major) or one per 64-wide box
-// (MN-major), multicast when the slice feeds several CTAs.
-//   K-major operand (rows x 64 K, 128-byte rows): slice = a band of rows.
-//   MN-major operand (64 K rows per 64-wide MN box): slice = a band of K rows of every box.
+// One operand's producer loop (run by one thread). Per k-block (BK wide): wait
+// until the stage is released by every CTA this thread writes into, arm each
+// receiver's full barrier with the bytes of this thread's slice (through mapa
+// for peers), then issue the slice, multicast when it feeds several CTAs.
+// Shared-memory tile layouts (128-byte swizzle throughout):
+//   K-major (rows x BK): BK/64 atoms, each rows x 128 bytes, atom after atom.
+//     With the 4-D k-split map one load fills any run of whole atoms, so a
+//     group of `parts` issuers splits the tile by atoms first (parts <= BK/64)
+//     and then by rows within an atom: one TMA load per issuer per stage.
+//     Without it (K not a multiple of 64; BK = 64) a slice is a band of rows.
+//   MN-major (BK x rows): rows/64 boxes of BK K-rows x 128 bytes; a slice is a
+//     band of K rows of every box (one TMA load per box).
 struct OperandPlan {
     const CUtensorMap* tmap;
     uint32_t tile0;        // shared address of stage 0's tile
     uint32_t tile_bytes;   // per stage
     int rows;              // MN extent of the tile held by this CTA
     int mn_major;
+    int kmap4;             // K-major with the 4-D k-split map
     int slice, parts;      // this CTA's slice index and the group size
     uint32_t mask;         // receivers (multicast) or just this CTA
 };
 
-template <int G>
+template <int G, int BK>
+__device__ __forceinline__ void tma_issue(const OperandPlan& op, bool mcast, uint32_t dst, uint32_t bar, int x, int y,
+                                          int z, int w, bool four_d) {
+    if (four_d) {
+        if (G == 1) {
+            if (mcast) tma_load_4d_mcast(dst, op.tmap, bar, x, y, z, w, (uint16_t)op.mask);
+            else       tma_load_4d(dst, op.tmap, bar, x, y, z, w);
+        } else {
+            if (mcast) tma_load_4d_pair_mcast(dst, op.tmap, bar, x, y, z, w, (uint16_t)op.mask);
+            else       tma_load_4d_pair(dst, op.tmap, bar, x, y, z, w);
+        }
+    } else {
+        if (G == 1) {
+            if (mcast) tma_load_3d_mcast(dst, op.tmap, bar, x, y, z, (uint16_t)op.mask);
+            else       tma_load_3d(dst, op.tmap, bar, x, y, z);
+        } else {
+            if (mcast) tma_load_3d_pair_mcast(dst, op.tmap, bar, x, y, z, (uint16_t)op.mask);
+            else       tma_load_3d_pair(dst, op.tmap, bar, x, y, z);
+        }
+    }
+}
+
+template <int G, int BK>
 __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan& op, bool is_a, uint32_t full0,
                                         uint32_t empty0, uint32_t rank, uint32_t leader, int cx, int cy, int rx,
                                         int ry, int BNv, int BN_CTAv, volatile int* abort_flag,
                                         long long first_tile, long long tile_stride, int S) {
+    constexpr int NAT = BK / ATOM_K;             // swizzle atoms per stage along K
     // Arm targets: the barrier that counts each receiver's bytes (the receiver
-    // itself, or its pair's even CTA), resolved once.
-    // Indexed by receiver rank with compile-time indices so it stays in registers.
+    // itself, or its pair's even CTA), resolved once and indexed by receiver
+    // rank with compile-time indices so the table stays in registers.
     uint32_t arm_addr[8];
 #pragma unroll
     for (int d = 0; d < 8; ++d)
@@ -192,9 +221,25 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     const uint32_t slice_bytes = op.tile_bytes / (uint32_t)op.parts;
     const uint32_t tma_bar0 = (G == 2) ? mapa(full0, leader) : full0;
     const bool mcast = op.parts > 1;
-    const int kr = BLOCK_K / op.parts;           // MN-major: K rows per slice
-    const int rr = op.rows / op.parts;           // K-major: MN rows per slice
-    const uint32_t slice_off = op.mn_major ? (uint32_t)(op.slice * kr * 128) : (uint32_t)(op.slice * rr * 128);
+    // This issuer's part of the tile.
+    int atom0 = 0, r0 = 0, k_rows = BK;
+    uint32_t slice_off;
+    if (op.mn_major) {
+        k_rows = BK / op.parts;
+        slice_off = (uint32_t)(op.slice * k_rows * 128);
+    } else if (op.kmap4) {
+        if (op.parts <= NAT) {
+            atom0 = op.slice * (NAT / op.parts);
+        } else {
+            const int rparts = op.parts / NAT;
+            atom0 = op.slice / rparts;
+            r0 = (op.slice % rparts) * (op.rows / rparts);
+        }
+        slice_off = (uint32_t)(atom0 * op.rows * 128 + r0 * 128);
+    } else {
+        r0 = op.slice * (op.rows / op.parts);
+        slice_off = (uint32_t)(r0 * 128);
+    }
     bool extra_tx = is_a && (p.debug_flags & 1) != 0;
     int stage = 0;
     uint32_t phase = 0;
@@ -217,29 +262,15 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
             }
             const uint32_t bar = tma_bar0 + 8u * stage;
             const uint32_t dst = op.tile0 + stage * op.tile_bytes + slice_off;
-            const int k0 = kb * BLOCK_K;
-            if (!op.mn_major) {
-                const int y = mn0 + op.slice * rr;
-                if (G == 1) {
-                    if (mcast) tma_load_3d_mcast(dst, op.tmap, bar, k0, y, tc.b, (uint16_t)op.mask);
-                    else       tma_load_3d(dst, op.tmap, bar, k0, y, tc.b);
-                } else {
-                    if (mcast) tma_load_3d_pair_mcast(dst, op.tmap, bar, k0, y, tc.b, (uint16_t)op.mask);
-                    else       tma_load_3d_pair(dst, op.tmap, bar, k0, y, tc.b);
-                }
+            if (op.mn_major) {
+                const int y = kb * BK + op.slice * k_rows;
+                for (int box = 0; box < op.rows / 64; ++box)
+                    tma_issue<G, BK>(op, mcast, dst + (uint32_t)(box * BK * 128), bar, mn0 + box * 64, y, tc.b, 0,
+                                     false);
+            } else if (op.kmap4) {
+                tma_issue<G, BK>(op, mcast, dst, bar, 0, mn0 + r0, kb * NAT + atom0, tc.b, true);
             } else {
-                const int y = k0 + op.slice * kr;
-                for (int box = 0; box < op.rows / 64; ++box) {
-                    const uint32_t d = dst + (uint32_t)(box * BOX_BYTES);
-                    const int x = mn0 + box * 64;
-                    if (G == 1) {
-                        if (mcast) tma_load_3d_mcast(d, op.tmap, bar, x, y, tc.b, (uint16_t)op.mask);
-                        else       tma_load_3d(d, op.tmap, bar, x, y, tc.b);
-                    } else {
-                        if (mcast) tma_load_3d_pair_mcast(d, op.tmap, bar, x, y, tc.b, (uint16_t)op.mask);
-                        else       tma_load_3d_pair(d, op.tmap, bar, x, y, tc.b);
-                    }
-                }
+                tma_issue<G, BK>(op, mcast, dst, bar, kb * BK, mn0 + r0, tc.b, 0, false);
             }
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -254,13 +285,14 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     return true;
 }
 
-template <int BN, int G>
+template <int BN, int G, int BK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
     constexpr int BN_CTA = BN / G;                      // B columns held per CTA
-    constexpr uint32_t A_BYTES = BLOCK_M * BLOCK_K * 2;
-    constexpr uint32_t B_BYTES = BN_CTA * BLOCK_K * 2;
+    constexpr uint32_t A_BYTES = BLOCK_M * BK * 2;
+    constexpr uint32_t B_BYTES = BN_CTA * BK * 2;
+    static_assert(BK == 64 || BK == 128, "a stage is one or two 128-byte swizzle atoms deep");
     constexpr uint32_t TMEM_COLS = 2 * BN;              // two accumulators
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
     static_assert(BN_CTA % 64 == 0, "B slab must be whole 64-column boxes");
@@ -329,12 +361,12 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             OperandPlan op;
             if (is_a) {
                 prefetch_tmap(&tmA);
-                op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, idxA, gA, maskA};
+                op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, p.a_kmap4, idxA, gA, maskA};
             } else {
                 prefetch_tmap(&tmB);
-                op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, idxB, gB, maskB};
+                op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB};
             }
-            produce<G>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
+            produce<G, BK>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
                        BN, BN_CTA, abort_flag, first_tile, tile_stride, S);
         }
     } else if (warp == 1) {
@@ -353,10 +385,18 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const bool local_only = (empty_mask == (1u << rank));
             // Descriptors advance by adding (byte offset >> 4) to the start-address
             // field (shared addresses stay below 256 KB, so the field cannot carry).
-            const uint32_t a_kstep = p.a_mn_major ? (16u * 128u) >> 4 : 32u >> 4;   // per 16-element K step
-            const uint32_t b_kstep = p.b_mn_major ? (16u * 128u) >> 4 : 32u >> 4;
-            const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA), p.a_mn_major != 0);
-            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sB), p.b_mn_major != 0);
+            // K step k (16 elements): MN-major -> 16 K rows further (k * 2048 B);
+            // K-major -> atom k/4 (rows * 128 B apart), 32 B into the row per step.
+            uint32_t a_koff[BK / 16], b_koff[BK / 16];
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+                a_koff[k] = p.a_mn_major ? (uint32_t)(k * 2048) >> 4
+                                         : (uint32_t)((k >> 2) * BLOCK_M * 128 + (k & 3) * 32) >> 4;
+                b_koff[k] = p.b_mn_major ? (uint32_t)(k * 2048) >> 4
+                                         : (uint32_t)((k >> 2) * BN_CTA * 128 + (k & 3) * 32) >> 4;
+            }
+            const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA), p.a_mn_major != 0, BK * 128);
+            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sB), p.b_mn_major != 0, BK * 128);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t local_tile = 0;
@@ -375,8 +415,8 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint64_t a_st = adesc0 + ((stage * A_BYTES) >> 4);
                     const uint64_t b_st = bdesc0 + ((stage * B_BYTES) >> 4);
 #pragma unroll
-                    for (int k = 0; k < BLOCK_K / 16; ++k)
-                        mma_bf16<G>(d_tmem, a_st + k * a_kstep, b_st + k * b_kstep, idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16<G>(d_tmem, a_st + a_koff[k], b_st + b_koff[k], idesc, (kb | k) != 0 ? 1u : 0u);
                     const uint32_t eb = smem_u32(&empty_bar[stage]);
                     if (local_only) mma_commit<G>(eb);
                     else            mma_commit_mcast<G>(eb, (uint16_t)empty_mask);

@@ -157,6 +157,35 @@ __device__ __forceinline__ void tma_load_3d_pair_mcast(uint32_t dst, const void*
         " [%0], [%1, {%3, %4, %5}], [%2], %6;"
         :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask) : "memory");
 }
+// 4-D variants (the k-split view of a K-major operand: {64 K, rows, K/64, batch}).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_mcast(uint32_t dst, const void* tmap, uint32_t bar,
+                                                  int32_t x, int32_t y, int32_t z, int32_t w, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair_mcast(uint32_t dst, const void* tmap, uint32_t bar,
+                                                       int32_t x, int32_t y, int32_t z, int32_t w, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask) : "memory");
+}
 // 3-D tiled store from this CTA's shared memory (clipped at the tensor bounds).
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
                                              int32_t x, int32_t y, int32_t z) {
@@ -275,10 +304,10 @@ __device__ __forceinline__ void tmem_ld_wait() {
 //   bits 61-63  layout: 2 = 128-byte swizzle
 // K-major operand (K contiguous): the 16-element K step of one MMA stays inside
 // a 128-byte row; SBO = 1024 bytes between 8-row groups, LBO unused (16).
-// MN-major operand (M or N contiguous): 64-element MN atoms are LBO = 8192
-// bytes apart (one 64-row K box each), 8-row K groups SBO = 1024 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, bool mn_major) {
-    const uint64_t lbo = mn_major ? 8192u : 16u;
+// MN-major operand (M or N contiguous): 64-element MN atoms are LBO = BK*128
+// bytes apart (one BK-row K box each), 8-row K groups SBO = 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, bool mn_major, uint32_t mn_lbo) {
+    const uint64_t lbo = mn_major ? mn_lbo : 16u;
     const uint64_t sbo = 1024u;
     uint64_t d = 0;
     d |= (uint64_t)((addr >> 4) & 0x3FFFu);

@@ -42,7 +42,7 @@ GEMM_DEBUG_EXTRA_TX = 1
 class gemm_options_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "mode", "mcast_a", "mcast_b", "cluster_m", "cluster_n", "cta_group", "layout_a", "layout_b",
-        "layout_c", "out_type", "block_n", "stages", "max_clusters", "group_m")] + [
+        "layout_c", "out_type", "block_n", "block_k", "stages", "max_clusters", "group_m")] + [
         ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_int)]
 
 

@@ -66,9 +66,9 @@ WORKLOADS = {
     "scores_8x16x4096x4096x128": Workload(
         "scores_8x16x4096x4096x128", 4096, 4096, 128, batch=128, dist="normal", layout_a="row",
         layout_b="col", out="f32",
-        options=dict(mode="mcast", mcast_b=1, cluster_m=2, cluster_n=1),
+        options=dict(mode="mcast", mcast_b=1, cluster_m=4, cluster_n=1),
         description="attention scores S = Q K^T, batch 8 x heads 16, seq 4096, head dim 128, "
-                    "N(0,1) bf16 Q/K, fp32 S, K tile multicast across the Q-tile CTAs"),
+                    "N(0,1) bf16 Q/K, fp32 S, each K tile multicast across the 4 Q-tile CTAs of a cluster"),
     "skinny_16384x128x8192": Workload(
         "skinny_16384x128x8192", 16384, 128, 8192, dist="uniform",
         options=dict(mode="mcast", mcast_b=1, cluster_m=4, cluster_n=1, block_n=128),

@@ -82,6 +82,8 @@ typedef struct {
     int layout_c;       /* gemm_layout_t of C (M x N) */
     int out_type;       /* gemm_out_t: element type of C */
     int block_n;        /* N extent of one MMA tile: 0 (auto = 256), 128 or 256 */
+    int block_k;        /* K extent of one pipeline stage: 0 (auto), 64 or 128; 128 needs K a
+                           multiple of 64 when A or B is K-major (auto picks 64 otherwise) */
     int stages;         /* shared-memory pipeline depth; 0 = as many as fit */
     int max_clusters;   /* cap on the persistent grid, in clusters; 0 = as many as are co-resident */
     int group_m;        /* raster band height, in cluster tiles along M; 0 = 8 */
@@ -94,7 +96,7 @@ typedef struct {
 typedef struct {
     int block_m;        /* rows of C per CTA (128) */
     int block_n;        /* columns of C per MMA tile */
-    int block_k;        /* K per pipeline stage (64) */
+    int block_k;        /* K per pipeline stage (64 or 128) */
     int stages;         /* pipeline depth */
     int smem_bytes;     /* dynamic shared memory per CTA */
     int cluster_m, cluster_n;   /* after the column-major-C transpose, if any */

@@ -72,7 +72,10 @@ def test_plan_4096_cluster2x1(lib):
 
 def test_plan_pair_with_b_multicast(lib):
     s, p = plan(lib, 8192, 8192, 8192, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1)
-    assert s == 0 and p.group_b == 2 and p.group_a == 1 and p.stages == 6
+    assert s == 0 and p.group_b == 2 and p.group_a == 1
+    assert p.block_k == 128 and p.stages == 3          # 64 KB stages: three fit
+    s, p = plan(lib, 8192, 8192, 8192, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1, block_k=64)
+    assert s == 0 and p.block_k == 64 and p.stages == 6
     from dense_gemm_cluster_gb300 import traffic
     uni = traffic.l2_to_sm_operand_bytes(8192, 8192, 8192)
     assert uni == 2 * p.l2_to_sm_operand_bytes
@@ -107,6 +110,20 @@ def test_plan_rejects_bad_sizes(lib):
     assert plan(lib, 1 << 31, 4, 4)[0] == 1
     s, p = plan(lib, 0, 0, 0)
     assert s == 0 and p.tiles == 0
+
+
+def test_block_k_choice(lib):
+    # K-major operands with K not a multiple of 64 cannot use the k-split map
+    s, p = plan(lib, 512, 512, 200, cta_group=2, cluster_m=2)
+    assert s == 0 and p.block_k == 64
+    assert plan(lib, 512, 512, 200, cta_group=2, cluster_m=2, block_k=128)[0] == 2
+    # both operands MN-major: any K works with 128-wide stages
+    s, p = plan(lib, 512, 512, 200, cta_group=2, cluster_m=2, layout_a="col", layout_b="row", block_k=128)
+    assert s == 0 and p.block_k == 128
+    # 128x256 single-CTA tiles: 96 KB stages leave room for two only, so auto keeps 64
+    s, p = plan(lib, 4096, 4096, 4096)
+    assert p.block_k == 64 and p.stages == 4
+    assert plan(lib, 64, 64, 64, block_k=32)[0] == 2
 
 
 def test_unicast_mode_ignores_multicast_flags(lib):

@@ -129,3 +129,12 @@ def test_gemm_4096_sampled(G):
     assert np.isfinite(got).all()
     assert 0.5 < np.std(got) / np.sqrt(4096 / 9.0) < 1.5
     g.close()
+
+
+@pytest.mark.parametrize("cm,cn,ma,mb", [(1, 1, 0, 0), (2, 1, 0, 1), (1, 4, 1, 0), (4, 2, 1, 1), (8, 1, 0, 1)])
+@pytest.mark.parametrize("la,lb", [("row", "col"), ("col", "row")])
+def test_128_wide_stages_single_cta_tiles(G, cm, cn, ma, mb, la, lb):
+    # K = 576 = 4.5 stages of 128 (half-empty last stage); 128-wide tiles keep three stages
+    p = Problem(900, 1000, 576, la=la, lb=lb, out="f32", seed=8)
+    got = _run(G, p, mode="mcast", mcast_a=ma, mcast_b=mb, cluster_m=cm, cluster_n=cn, block_n=128, block_k=128)
+    assert_close(got, p.reference(), 576, "f32", f"bk128 {cm}x{cn} A{ma} B{mb} {la}/{lb}")

@@ -65,3 +65,24 @@ def test_pair_persistent_few_clusters(G):
     p = Problem(1536, 1024, 512, seed=15)
     got = _run(G, p, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1, max_clusters=2, stages=3)
     assert_close(got, p.reference(), 512, "bf16", "pair persistent")
+
+
+@pytest.mark.parametrize("la,lb", [("row", "col"), ("row", "row"), ("col", "col")])
+@pytest.mark.parametrize("cm,cn,ma,mb,bn", [(2, 1, 0, 0, 256), (4, 1, 0, 1, 256), (8, 1, 0, 1, 128),
+                                            (2, 4, 1, 0, 256), (4, 2, 1, 1, 128)])
+def test_pair_128_wide_stages(G, la, lb, cm, cn, ma, mb, bn):
+    # K = 448 = 3.5 stages of 128: the last stage's second atom lies past K and must read as zeros
+    p = Problem(700, 1100, 448, la=la, lb=lb, out="bf16", seed=16)
+    base = _run(G, p, cta_group=2, cluster_m=2, block_k=64)
+    got = _run(G, p, cta_group=2, cluster_m=cm, cluster_n=cn, mode="mcast", mcast_a=ma, mcast_b=mb,
+               block_n=bn, block_k=128)
+    assert_close(got, p.reference(), 448, "bf16", f"pair bk128 {la}/{lb} cluster {cm}x{cn} A{ma} B{mb} bn{bn}")
+    if bn == 256:
+        assert np.array_equal(got, base)   # same MMA sequence per k: bit-identical
+
+
+@pytest.mark.parametrize("K", [200, 65, 1])
+def test_pair_auto_stage_width_with_ragged_k(G, K):
+    p = Problem(300, 520, K, la="row", lb="col", out="f32", seed=17)
+    got = _run(G, p, cta_group=2, cluster_m=2)
+    assert_close(got, p.reference(), K, "f32", f"pair ragged K={K}")
