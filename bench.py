@@ -39,6 +39,7 @@ from dense_gemm_cluster_gb300.workloads import DEFAULT, WORKLOADS, Workload  # n
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense-BF16 peak; L2→SM bytes vs unicast"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 << 20          # GB300 L2 (126 MiB usable); inputs above this need no flush
 KERNEL_SOURCES = ["dense_gemm_cluster_gb300/csrc/gemm_kernel.cuh", "dense_gemm_cluster_gb300/csrc/ptx.cuh",
                   "dense_gemm_cluster_gb300/csrc/gemm_host.cu"]
 
@@ -328,7 +329,12 @@ def bench_ours(args, w: Workload):
 
     p = DeviceProblem(w, device)
     stream = torch.cuda.current_stream(device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    input_bytes = w.min_hbm_bytes()
+    needs_flush = input_bytes <= L2_BYTES
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device) if needs_flush else None
+    # A read after the write leaves L2 holding clean lines, so the timed kernel
+    # does not pay for writing back the flush buffer.
+    clean = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=device) if needs_flush else None
 
     for _ in range(max(3, args.warmup)):
         run_once(g, p, stream)
@@ -342,7 +348,9 @@ def bench_ours(args, w: Workload):
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            flush.fill_(float(i))                      # evicts the operands from L2
+            if needs_flush:
+                flush.fill_(float(i))                  # evicts the operands from L2
+                clean.sum()
             starts[i].record(stream)
             run_once(g, p, stream)
             ends[i].record(stream)
@@ -388,7 +396,9 @@ def bench_ours(args, w: Workload):
                    "beta": w.beta, "mode": opts, "cta_group": plan.cta_group, "block": [plan.block_m, plan.block_n,
                                                                                         plan.block_k],
                    "stages": plan.stages, "cluster": [plan.cluster_m, plan.cluster_n],
-                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "l2": (f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write, then a "
+                          f"{L2_FLUSH_BYTES >> 21} MB read)" if needs_flush else
+                          f"no flush: the inputs ({input_bytes >> 20} MB) are larger than L2"),
                    "description": w.description},
         "roofline": roofline,
         "l2_to_sm_operand_bytes": {"analytic": plan.l2_to_sm_operand_bytes,
@@ -456,10 +466,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch count of a batched workload (smaller profiling captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     w = WORKLOADS[args.workload]
+    if args.batch:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch, name=f"{w.name}[batch={args.batch}]")
     if args.impl == "reference":
         return bench_reference(args, w)
     return bench_ours(args, w)

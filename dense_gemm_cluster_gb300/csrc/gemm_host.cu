@@ -73,6 +73,8 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
         return fail(err, GEMM_ERR_UNSUPPORTED, "block_k must be 0, 64 or 128");
     if (o.group_m < 0 || o.max_clusters < 0 || o.stages < 0)
         return fail(err, GEMM_ERR_INVALID_ARG, "group_m, max_clusters and stages must be >= 0");
+    if (o.schedule < 0 || o.schedule > 2)
+        return fail(err, GEMM_ERR_INVALID_ARG, "schedule must be 0 (auto), 1 (whole tiles) or 2 (stream-K tail)");
     if (M < 0 || N < 0 || K < 0 || batch < 0)
         return fail(err, GEMM_ERR_INVALID_ARG, "negative size");
     if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) || batch >= (1ll << 31))
@@ -95,8 +97,9 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
 
     const int BN = o.block_n ? o.block_n : 256;
     // 1024 for aligning the dynamic base, the epilogue staging, then per stage a
-    // full and an empty barrier, plus 5 barriers, the TMEM address and the abort flag.
-    const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 5 * 8 + 16;
+    // full and an empty barrier, plus 5 barriers, the TMEM address, the abort flag
+    // and the epilogue warps' agreement words.
+    const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 5 * 8 + 32;
     auto stage_bytes_for = [&](int bk) { return dgc::BLOCK_M * bk * 2 + (BN / G) * bk * 2; };
     // Operands as launched (after the C^T transpose): K-major ones need K % 64 == 0
     // for the k-split map that 128-wide stages use.
@@ -152,7 +155,20 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     p.clusters = clusters;
     const int64_t k_pad = ceil_div(K, BK) * BK;
     p.l2_to_sm_operand_bytes = p.tiles * cm * cn * k_pad * 2 * (dgc::BLOCK_M / gA + (BN / G) / gB);
+    p.stream_k_tiles = 0;
     return GEMM_OK;
+}
+
+// Whole-tile waves and the stream-K tail for `tiles` cluster tiles on `clusters`
+// co-resident clusters. Returns the number of tiles processed whole (a multiple
+// of `clusters`); the rest are split by k-blocks.
+int64_t whole_tiles_for(int schedule, int64_t tiles, int64_t clusters, int num_kb, bool can_split) {
+    if (!can_split || schedule == 1 || num_kb < 2 || tiles == 0 || clusters <= 1) return tiles;
+    const int64_t waves = (tiles + clusters - 1) / clusters;
+    const double fill = (double)tiles / (double)(waves * clusters);
+    if (schedule == 0 && fill >= 0.9) return tiles;
+    const int64_t full = tiles / clusters;
+    return (full > 0 ? full - 1 : 0) * clusters;
 }
 
 template <int BN, int G, int BK>
@@ -202,6 +218,12 @@ struct gemm_handle_s {
     void* stage_ptr[3] = {nullptr, nullptr, nullptr};
     size_t stage_cap[3] = {0, 0, 0};
     int64_t launches = 0;
+    bool no_alloc = false;      // set on the stack handle of gemm_run_noalloc: never allocate
+    float* workspace = nullptr; // stream-K partial slots
+    unsigned int* flags = nullptr;
+    size_t workspace_bytes = 0;
+    size_t flag_count = 0;
+    unsigned int epoch = 0;
     bool smem_set[2][2][2] = {};
     int occ_key[2][2][2][9];    // cached max active clusters per (BN, G, BK, cluster size)
 };
@@ -238,7 +260,11 @@ extern "C" gemm_status_t gemm_plan(const gemm_options_t* opt, int64_t M, int64_t
         return fail(nullptr, GEMM_ERR_INVALID_ARG, "gemm_plan needs options, a plan and sm_count > 0");
     Resolved r;
     gemm_status_t s = resolve(*opt, M, N, K, batch, sm_count, r, nullptr);
-    if (s == GEMM_OK) *plan = r.pub;
+    if (s == GEMM_OK) {
+        *plan = r.pub;
+        const int num_kb = (int)ceil_div(K, r.pub.block_k);
+        plan->stream_k_tiles = r.pub.tiles - whole_tiles_for(opt->schedule, r.pub.tiles, r.pub.clusters, num_kb, true);
+    }
     return s;
 }
 
@@ -298,6 +324,8 @@ extern "C" gemm_status_t gemm_destroy(gemm_handle_t h) {
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
     if (h->d_status) cudaFree(h->d_status);
+    if (h->workspace) cudaFree(h->workspace);
+    if (h->flags) cudaFree(h->flags);
     for (int i = 0; i < 3; ++i)
         if (h->stage_ptr[i]) cudaFree(h->stage_ptr[i]);
     cudaSetDevice(prev);
@@ -536,6 +564,40 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     }
     int64_t clusters = pl.clusters < occ ? pl.clusters : occ;
     cfg.gridDim = dim3((unsigned)(clusters * cs), 1, 1);
+    // Stream-K tail (needs the co-residency the occupancy cap guarantees, and a workspace).
+    if (o.schedule == 2 && h->no_alloc)
+        return fail(&h->err, GEMM_ERR_UNSUPPORTED, "the stream-K tail needs a workspace; gemm_run_noalloc runs whole tiles");
+    kp.dp_tiles = whole_tiles_for(o.schedule, pl.tiles, clusters, kp.num_kb, !h->no_alloc);
+    kp.sk_iters = (pl.tiles - kp.dp_tiles) * kp.num_kb;
+    if (kp.sk_iters > 0) {
+        const size_t slots = (size_t)(clusters * cs);
+        const size_t ws_bytes = slots * dgc::BLOCK_M * BN * sizeof(float);
+        if (ws_bytes > h->workspace_bytes) {
+            if (h->workspace) cudaFree(h->workspace);
+            h->workspace = nullptr;
+            h->workspace_bytes = 0;
+            cudaError_t e = cudaMalloc(&h->workspace, ws_bytes);
+            if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "stream-K workspace: %s", cudaGetErrorString(e));
+            h->workspace_bytes = ws_bytes;
+        }
+        if (slots > h->flag_count) {
+            if (h->flags) cudaFree(h->flags);
+            h->flags = nullptr;
+            h->flag_count = 0;
+            cudaError_t e = cudaMalloc(&h->flags, slots * sizeof(unsigned int));
+            if (e == cudaSuccess) e = cudaMemset(h->flags, 0, slots * sizeof(unsigned int));
+            if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "stream-K flags: %s", cudaGetErrorString(e));
+            h->flag_count = slots;
+            h->epoch = 0;
+        }
+        if (++h->epoch == 0) {       // flags hold epochs; 0 means "never written"
+            cudaMemsetAsync(h->flags, 0, h->flag_count * sizeof(unsigned int), stream);
+            h->epoch = 1;
+        }
+        kp.workspace = h->workspace;
+        kp.flags = h->flags;
+        kp.epoch = h->epoch;
+    }
     void* args[] = {&tmA, &tmB, &tmC, &kp};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "cudaLaunchKernelEx: %s", cudaGetErrorString(e));
@@ -718,6 +780,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const gemm_options_t* opt, int device,
         local.opt = *opt;
         if (local.opt.wait_timeout_ns == 0) local.opt.wait_timeout_ns = kDefaultTimeoutNs;
         local.device = device;
+        local.no_alloc = true;
         local.sm_count = d.sm_count;
         local.d_status = static_cast<unsigned int*>(d.scratch);
         local.encode = d.encode;

@@ -63,6 +63,7 @@ enum : uint32_t {
     ERR_WAIT_TMEM_EMPTY = 3, // MMA waiting for the epilogue to free an accumulator
     ERR_WAIT_TMEM_FULL = 4,  // epilogue waiting for an accumulator
     ERR_WAIT_DRAIN = 5,      // teardown waiting for in-flight MMAs
+    ERR_WAIT_PARTIAL = 6,    // stream-K finisher waiting for another cluster's partial
 };
 
 struct KernelParams {
@@ -84,6 +85,13 @@ struct KernelParams {
     long long ldc, stride_c; // elements
     unsigned int* status;    // 4 words: code, detail, block, tile
     unsigned long long timeout_ns;
+    // Stream-K tail: tiles [0, dp_tiles) go whole to clusters by a static stride;
+    // the sk_iters k-blocks of the remaining tiles are split evenly over the clusters.
+    long long dp_tiles;
+    long long sk_iters;
+    float* workspace;        // one BLOCK_M x BN fp32 partial slot per CTA of the grid
+    unsigned int* flags;     // per slot: the epoch whose partial the slot holds
+    unsigned int epoch;      // this launch's epoch (never 0)
 };
 
 struct TileCoord {
@@ -104,6 +112,73 @@ __device__ __forceinline__ TileCoord tile_coord(const KernelParams& p, long long
     c.ctn = local / gsz;
     return c;
 }
+
+// One unit of work of a cluster: k-blocks [kb0, kb1) of cluster tile `tile`.
+//   WHOLE:    the full K range; the epilogue stores C.
+//   PARTIAL:  a later part of a tile whose first k-block another cluster owns;
+//             the epilogue writes the fp32 partial to this CTA's workspace slot
+//             and raises its flag.
+//   FINISHER: the first part of a tile whose rest other clusters compute; the
+//             epilogue adds their partials (in cluster order) before storing C.
+enum : int { WORK_WHOLE = 0, WORK_PARTIAL = 1, WORK_FINISHER = 2 };
+
+struct Work {
+    long long tile;
+    int kb0, kb1;
+    int kind;
+    int contrib_first, contrib_count;   // FINISHER: clusters whose slots hold the rest
+};
+
+// Static persistent schedule with a stream-K tail ("Clusters, distributed
+// shared memory & cluster launch control", section "The second wall": a fixed
+// stride leaves SMs idle in the last wave when tiles do not divide evenly;
+// splitting the last tiles' k-blocks evenly removes that tail). Every role of
+// every CTA of a cluster walks the same sequence.
+struct WorkIter {
+    long long dp_next, sk_it, sk_end, cid, ncl, base, rem;
+
+    __device__ void init(const KernelParams& p, long long cluster, long long clusters) {
+        cid = cluster;
+        ncl = clusters;
+        dp_next = cluster;
+        base = p.sk_iters / clusters;
+        rem = p.sk_iters % clusters;
+        sk_it = start_of(cluster);
+        sk_end = start_of(cluster + 1);
+    }
+    __device__ long long start_of(long long c) const { return c * base + (c < rem ? c : rem); }
+
+    __device__ bool next(const KernelParams& p, Work& w) {
+        if (dp_next < p.dp_tiles) {
+            w.tile = dp_next;
+            w.kb0 = 0;
+            w.kb1 = p.num_kb;
+            w.kind = WORK_WHOLE;
+            dp_next += ncl;
+            return true;
+        }
+        if (sk_it >= sk_end) return false;
+        const long long rel = sk_it / p.num_kb;
+        w.tile = p.dp_tiles + rel;
+        w.kb0 = (int)(sk_it - rel * p.num_kb);
+        const long long left = sk_end - sk_it;
+        w.kb1 = (int)((long long)(p.num_kb - w.kb0) < left ? p.num_kb : w.kb0 + left);
+        if (w.kb0 > 0) {
+            w.kind = WORK_PARTIAL;
+        } else if (w.kb1 < p.num_kb) {
+            w.kind = WORK_FINISHER;
+            const long long tile_end = (rel + 1) * p.num_kb;
+            w.contrib_first = (int)(cid + 1);
+            int n = 0;
+            while (cid + 1 + n < ncl && start_of(cid + 1 + n) < tile_end) ++n;
+            w.contrib_count = n;
+        } else {
+            w.kind = WORK_WHOLE;
+        }
+        sk_it += w.kb1 - w.kb0;
+        return true;
+    }
+};
 
 __device__ __noinline__ void report_timeout(const KernelParams& p, uint32_t code, uint32_t detail,
                                             long long tile) {
@@ -209,7 +284,7 @@ template <int G, int BK>
 __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan& op, bool is_a, uint32_t full0,
                                         uint32_t empty0, uint32_t rank, uint32_t leader, int cx, int cy, int rx,
                                         int ry, int BNv, int BN_CTAv, volatile int* abort_flag,
-                                        long long first_tile, long long tile_stride, int S) {
+                                        long long cluster, long long clusters, int S) {
     constexpr int NAT = BK / ATOM_K;             // swizzle atoms per stage along K
     // Arm targets: the barrier that counts each receiver's bytes (the receiver
     // itself, or its pair's even CTA), resolved once and indexed by receiver
@@ -243,11 +318,15 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     bool extra_tx = is_a && (p.debug_flags & 1) != 0;
     int stage = 0;
     uint32_t phase = 0;
-    for (long long t = first_tile; t < p.total_tiles; t += tile_stride) {
+    WorkIter wi;
+    wi.init(p, cluster, clusters);
+    Work w;
+    while (wi.next(p, w)) {
+        const long long t = w.tile;
         const TileCoord tc = tile_coord(p, t);
         const int mn0 = is_a ? (tc.ctm * cx + rx) * BLOCK_M
                              : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, p, abort_flag, ERR_WAIT_EMPTY, (uint32_t)stage, t))
                 return false;
 #pragma unroll
@@ -311,6 +390,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t* drain_bar = bars + 2 * S + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // 4 entries, one per epilogue warp
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -351,8 +431,8 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const long long first_tile = cluster_id_x();
-    const long long tile_stride = num_clusters_x();
+    const long long cluster = cluster_id_x();
+    const long long clusters = num_clusters_x();
 
     if (warp == 0 || warp == 6) {
         // ------------------------------------------------------------ producers (A: warp 0, B: warp 6)
@@ -367,7 +447,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB};
             }
             produce<G, BK>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
-                       BN, BN_CTA, abort_flag, first_tile, tile_stride, S);
+                       BN, BN_CTA, abort_flag, cluster, clusters, S);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -401,14 +481,18 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             uint32_t local_tile = 0;
             bool ok = true;
-            for (long long t = first_tile; ok && t < p.total_tiles; t += tile_stride, ++local_tile) {
+            WorkIter wi;
+            wi.init(p, cluster, clusters);
+            Work w;
+            for (; ok && wi.next(p, w); ++local_tile) {
+                const long long t = w.tile;
                 const uint32_t acc = local_tile & 1u;
                 const uint32_t acc_phase = (local_tile >> 1) & 1u;
                 if (!wait_bounded<G == 2>(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, p, abort_flag,
                                           ERR_WAIT_TMEM_EMPTY, acc, t)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(smem_u32(&full_bar[stage]), phase, p, abort_flag,
                                       ERR_WAIT_FULL, (uint32_t)stage, t)) { ok = false; break; }
                     tc_fence_after();
@@ -416,7 +500,8 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint64_t b_st = bdesc0 + ((stage * B_BYTES) >> 4);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        mma_bf16<G>(d_tmem, a_st + a_koff[k], b_st + b_koff[k], idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_bf16<G>(d_tmem, a_st + a_koff[k], b_st + b_koff[k], idesc,
+                                    (kb > w.kb0 || k > 0) ? 1u : 0u);
                     const uint32_t eb = smem_u32(&empty_bar[stage]);
                     if (local_only) mma_commit<G>(eb);
                     else            mma_commit_mcast<G>(eb, (uint16_t)empty_mask);
@@ -443,19 +528,77 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int chunks = BN / CW;
 
         const bool use_beta = p.beta != 0.0f;
+        const int cs = cx * cy;
+        const long long slot = cluster * cs + rank;       // this CTA's stream-K workspace slot
         uint32_t local_tile = 0;
         uint32_t buf = 0;
-        for (long long t = first_tile; t < p.total_tiles; t += tile_stride, ++local_tile) {
+        WorkIter wi;
+        wi.init(p, cluster, clusters);
+        Work w;
+        for (; wi.next(p, w); ++local_tile) {
+            const long long t = w.tile;
             const uint32_t acc = local_tile & 1u;
             const uint32_t acc_phase = (local_tile >> 1) & 1u;
-            if (!wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, p, abort_flag,
-                              ERR_WAIT_TMEM_FULL, acc, t)) break;
+            const bool ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, p, abort_flag,
+                                         ERR_WAIT_TMEM_FULL, acc, t);
+            // The four epilogue warps agree on going on, so that none is ever left
+            // alone at the named barrier below after another has stopped.
+            if (lane == 0) epi_ok[ew] = ok ? 1 : 0;
+            epilogue_bar();
+            const bool all_ok = epi_ok[0] && epi_ok[1] && epi_ok[2] && epi_ok[3];
+            epilogue_bar();
+            if (!all_ok) break;
             tc_fence_after();
             const TileCoord tc = tile_coord(p, t);
             const int m0 = (tc.ctm * cx + rx) * BLOCK_M;
             const int n0 = (tc.ctn * cy + ry) * BN;
-            const int row = m0 + q * 32 + lane;           // global row this thread stores
+            const int trow = q * 32 + lane;               // row of the tile this thread owns
+            const int row = m0 + trow;                    // global row this thread stores
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            if (w.kind == WORK_PARTIAL) {
+                // Part of a tile another cluster finishes: park the fp32 partial.
+                float* dst = p.workspace + (slot * BLOCK_M + trow) * (long long)BN;
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(t_row + c * 32, r);
+                    tmem_ld_wait();
+                    if (c == BN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (G == 2) mbar_arrive_cluster(mapa(smem_u32(&tempty_bar[acc]), leader));
+                            else        mbar_arrive_local(smem_u32(&tempty_bar[acc]));
+                        }
+                    }
+                    float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                }
+                __threadfence();
+                epilogue_bar();
+                if (warp == 2 && lane == 0) st_release_gpu(&p.flags[slot], p.epoch);
+                continue;
+            }
+            if (w.kind == WORK_FINISHER) {
+                // Wait until every later contributor of this tile has parked its partial.
+                if (warp == 2 && lane == 0) {
+                    for (int i = 0; i < w.contrib_count; ++i) {
+                        const unsigned int* f = &p.flags[(long long)(w.contrib_first + i) * cs + rank];
+                        const uint64_t c0 = clock_cycles();
+                        while (ld_acquire_gpu(f) != p.epoch) {
+                            if (*abort_flag) break;
+                            if (clock_cycles() - c0 > 2ull * p.timeout_ns) {
+                                report_timeout(p, ERR_WAIT_PARTIAL, (uint32_t)(w.contrib_first + i), t);
+                                *abort_flag = 1;
+                                break;
+                            }
+                        }
+                    }
+                }
+                epilogue_bar();
+            }
             for (int c = 0; c < chunks; ++c) {
                 const int col0 = n0 + c * CW;
                 float v[64];
@@ -472,6 +615,25 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
+                }
+                if (w.kind == WORK_FINISHER) {
+                    // Add the other contributors' partials, in cluster order.
+                    const int nv = p.out_f32 ? 32 : 64;
+                    for (int i = 0; i < w.contrib_count; ++i) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            p.workspace + (((long long)(w.contrib_first + i) * cs + rank) * BLOCK_M + trow) *
+                                              (long long)BN + c * CW);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (4 * j < nv) {
+                                const float4 a = src[j];
+                                v[4 * j] += a.x;
+                                v[4 * j + 1] += a.y;
+                                v[4 * j + 2] += a.z;
+                                v[4 * j + 3] += a.w;
+                            }
+                        }
+                    }
                 }
                 if (c == chunks - 1) {
                     // All of this accumulator is in registers: hand it back.

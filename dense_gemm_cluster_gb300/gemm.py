@@ -42,7 +42,7 @@ GEMM_DEBUG_EXTRA_TX = 1
 class gemm_options_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "mode", "mcast_a", "mcast_b", "cluster_m", "cluster_n", "cta_group", "layout_a", "layout_b",
-        "layout_c", "out_type", "block_n", "block_k", "stages", "max_clusters", "group_m")] + [
+        "layout_c", "out_type", "block_n", "block_k", "stages", "max_clusters", "group_m", "schedule")] + [
         ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_int)]
 
 
@@ -50,7 +50,8 @@ class gemm_plan_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "block_m", "block_n", "block_k", "stages", "smem_bytes", "cluster_m", "cluster_n", "cta_group",
         "group_a", "group_b", "transposed")] + [
-        ("tiles", ctypes.c_int64), ("clusters", ctypes.c_int64), ("l2_to_sm_operand_bytes", ctypes.c_int64)]
+        ("tiles", ctypes.c_int64), ("clusters", ctypes.c_int64), ("l2_to_sm_operand_bytes", ctypes.c_int64),
+        ("stream_k_tiles", ctypes.c_int64)]
 
 
 _i64, _i32, _f32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
@@ -184,7 +185,7 @@ def make_options(**kw) -> gemm_options_t:
     out_type as "bf16"/"f32", mode as "unicast"/"mcast")."""
     o = gemm_options_default()
     names = {"row": GEMM_ROW_MAJOR, "col": GEMM_COL_MAJOR, "bf16": GEMM_OUT_BF16, "f32": GEMM_OUT_F32,
-             "unicast": GEMM_MODE_UNICAST, "mcast": GEMM_MODE_MCAST}
+             "unicast": GEMM_MODE_UNICAST, "mcast": GEMM_MODE_MCAST, "auto": 0, "dp": 1, "stream_k": 2}
     for k, v in kw.items():
         if not hasattr(o, k):
             raise TypeError(f"gemm_options_t has no field {k!r}")

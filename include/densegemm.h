@@ -87,6 +87,13 @@ typedef struct {
     int stages;         /* shared-memory pipeline depth; 0 = as many as fit */
     int max_clusters;   /* cap on the persistent grid, in clusters; 0 = as many as are co-resident */
     int group_m;        /* raster band height, in cluster tiles along M; 0 = 8 */
+    int schedule;       /* 0 = auto, 1 = whole tiles only, 2 = stream-K tail: the tiles
+                           left after the last full wave (between one and two waves'
+                           worth) are split by k-blocks evenly over all clusters, and the
+                           parts are summed in a fixed order. Auto uses it when whole tiles
+                           would leave the last wave under 90 % full. Needs a handle-owned
+                           workspace (one 128 x block_n fp32 tile per CTA), so
+                           gemm_run_noalloc always runs whole tiles. */
     uint64_t wait_timeout_ns; /* bound on every in-kernel wait, counted as 2 SM cycles per ns
                                  (this long at 2 GHz, longer at lower clocks); 0 = 2 s */
     int debug_flags;    /* 0, or GEMM_DEBUG_EXTRA_TX (tests only) */
@@ -107,6 +114,7 @@ typedef struct {
     int64_t tiles;      /* cluster tiles in the whole problem (all batches) */
     int64_t clusters;   /* persistent grid size in clusters (before the occupancy cap) */
     int64_t l2_to_sm_operand_bytes; /* analytic TMA operand fetches for the launch */
+    int64_t stream_k_tiles;   /* tiles split by k-blocks (0: whole tiles only) */
 } gemm_plan_t;
 
 /* Default options: unicast, 1x1 cluster, cta_group 1, A row-major, B column-major,
@@ -118,8 +126,8 @@ void gemm_options_default(gemm_options_t *opt);
  * for an impossible mode (cluster > 8 CTAs, odd cluster_m with cta_group 2, a
  * multicast slice under 8 rows) and for any multicast mode when the environment
  * variable WORLD_SIZE is above 1 (multi-GPU jobs run without cluster multicast).
- * The handle owns a 16-byte device status word and, after gemm_run_host, staging
- * buffers; gemm_destroy frees them. */
+ * The handle owns a 16-byte device status word and, once needed, the stream-K
+ * workspace and the gemm_run_host staging buffers; gemm_destroy frees them. */
 gemm_status_t gemm_create(gemm_handle_t *out, const gemm_options_t *opt, int device);
 
 /* C <- alpha * op(A) * op(B) + beta * C on `stream`, asynchronously.

@@ -129,3 +129,18 @@ def test_block_k_choice(lib):
 def test_unicast_mode_ignores_multicast_flags(lib):
     s, p = plan(lib, 512, 512, 512, mode="unicast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2)
     assert s == 0 and p.group_a == 1 and p.group_b == 1
+
+
+def test_plan_stream_k_tail(lib):
+    # 4096^3, 2x1 clusters: 256 cluster tiles on 76 clusters -> 3.37 waves; auto splits the tail
+    s, p = plan(lib, 4096, 4096, 4096, sm=152, mode="mcast", mcast_b=1, cluster_m=2)
+    assert s == 0 and p.clusters == 76
+    assert p.stream_k_tiles == 256 - 2 * 76
+    s, p = plan(lib, 4096, 4096, 4096, sm=152, mode="mcast", mcast_b=1, cluster_m=2, schedule="dp")
+    assert p.stream_k_tiles == 0
+    # a full last wave keeps whole tiles; a single k-block cannot be split
+    s, p = plan(lib, 128 * 152, 256, 4096, sm=152)
+    assert p.stream_k_tiles == 0
+    s, p = plan(lib, 4096, 4096, 64, sm=152)
+    assert p.stream_k_tiles == 0
+    assert plan(lib, 64, 64, 64, schedule=3)[0] == 1

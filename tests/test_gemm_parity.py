@@ -75,8 +75,8 @@ def test_alpha_beta(G, alpha, beta, out):
 @pytest.mark.parametrize("bn", [128, 256])
 def test_cluster_modes_match_oracle_and_unicast_bitwise(G, cm, cn, ma, mb, bn):
     p = Problem(1000, 1100, 448, la="row", lb="col", out="bf16", seed=5)
-    uni = _run(G, p, block_n=bn)
-    got = _run(G, p, mode="mcast", mcast_a=ma, mcast_b=mb, cluster_m=cm, cluster_n=cn, block_n=bn)
+    uni = _run(G, p, block_n=bn, schedule="dp")
+    got = _run(G, p, mode="mcast", mcast_a=ma, mcast_b=mb, cluster_m=cm, cluster_n=cn, block_n=bn, schedule="dp")
     assert_close(got, p.reference(), 448, "bf16", f"cluster {cm}x{cn} mcast A{ma} B{mb}")
     # multicast moves the same operand bytes: the product is bit-identical
     assert np.array_equal(got, uni)
@@ -138,3 +138,23 @@ def test_128_wide_stages_single_cta_tiles(G, cm, cn, ma, mb, la, lb):
     p = Problem(900, 1000, 576, la=la, lb=lb, out="f32", seed=8)
     got = _run(G, p, mode="mcast", mcast_a=ma, mcast_b=mb, cluster_m=cm, cluster_n=cn, block_n=128, block_k=128)
     assert_close(got, p.reference(), 576, "f32", f"bk128 {cm}x{cn} A{ma} B{mb} {la}/{lb}")
+
+
+@pytest.mark.parametrize("M,N,K,max_clusters,bn,out,beta", [
+    (1000, 1100, 448, 5, 256, "bf16", 0.0),     # 5 clusters, 20 tiles: a 5-tile tail split by k-blocks
+    (520, 384, 1024, 7, 128, "f32", 0.5),       # ragged tiles, beta read once by each finisher
+    (256, 256, 2048, 3, 256, "bf16", 1.0),      # 2 tiles over 3 clusters: every tile split
+    (129, 1000, 960, 6, 128, "f32", 0.0),       # many contributors per tile
+])
+def test_stream_k_tail_matches_oracle(G, M, N, K, max_clusters, bn, out, beta):
+    p = Problem(M, N, K, la="row", lb="col", out=out, beta=beta, seed=9)
+    got = _run(G, p, 1.0, beta, schedule="stream_k", max_clusters=max_clusters, block_n=bn)
+    assert_close(got, p.reference(1.0, beta), K, out, f"stream-K {M}x{N}x{K} on {max_clusters} clusters")
+
+
+def test_stream_k_with_multicast_clusters_is_deterministic(G):
+    p = Problem(1300, 1500, 704, la="col", lb="row", out="f32", seed=10)
+    a = _run(G, p, schedule="stream_k", mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2, max_clusters=9)
+    b = _run(G, p, schedule="stream_k", mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2, max_clusters=9)
+    assert_close(a, p.reference(), 704, "f32", "stream-K 2x2 multicast")
+    assert np.array_equal(a, b)          # partials are summed in a fixed order

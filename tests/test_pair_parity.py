@@ -42,8 +42,8 @@ def test_pair_unicast(G, bn, la, lb):
 @pytest.mark.parametrize("cm,cn,ma,mb", [(4, 1, 0, 1), (2, 2, 1, 0), (4, 2, 1, 1), (2, 4, 1, 0), (8, 1, 0, 1)])
 def test_pair_with_multicast_bitwise_equals_pair_unicast(G, cm, cn, ma, mb):
     p = Problem(1100, 1300, 512, la="row", lb="row", out="bf16", seed=12)
-    base = _run(G, p, cta_group=2, cluster_m=2, cluster_n=1)
-    got = _run(G, p, cta_group=2, cluster_m=cm, cluster_n=cn, mode="mcast", mcast_a=ma, mcast_b=mb)
+    base = _run(G, p, cta_group=2, cluster_m=2, cluster_n=1, schedule="dp")
+    got = _run(G, p, cta_group=2, cluster_m=cm, cluster_n=cn, mode="mcast", mcast_a=ma, mcast_b=mb, schedule="dp")
     assert_close(got, p.reference(), 512, "bf16", f"pair cluster {cm}x{cn} A{ma} B{mb}")
     assert np.array_equal(got, base)
 
@@ -73,9 +73,9 @@ def test_pair_persistent_few_clusters(G):
 def test_pair_128_wide_stages(G, la, lb, cm, cn, ma, mb, bn):
     # K = 448 = 3.5 stages of 128: the last stage's second atom lies past K and must read as zeros
     p = Problem(700, 1100, 448, la=la, lb=lb, out="bf16", seed=16)
-    base = _run(G, p, cta_group=2, cluster_m=2, block_k=64)
+    base = _run(G, p, cta_group=2, cluster_m=2, block_k=64, schedule="dp")
     got = _run(G, p, cta_group=2, cluster_m=cm, cluster_n=cn, mode="mcast", mcast_a=ma, mcast_b=mb,
-               block_n=bn, block_k=128)
+               block_n=bn, block_k=128, schedule="dp")
     assert_close(got, p.reference(), 448, "bf16", f"pair bk128 {la}/{lb} cluster {cm}x{cn} A{ma} B{mb} bn{bn}")
     if bn == 256:
         assert np.array_equal(got, base)   # same MMA sequence per k: bit-identical
@@ -86,3 +86,11 @@ def test_pair_auto_stage_width_with_ragged_k(G, K):
     p = Problem(300, 520, K, la="row", lb="col", out="f32", seed=17)
     got = _run(G, p, cta_group=2, cluster_m=2)
     assert_close(got, p.reference(), K, "f32", f"pair ragged K={K}")
+
+
+@pytest.mark.parametrize("cm,cn,ma,mb", [(2, 1, 0, 0), (4, 1, 0, 1), (2, 2, 1, 0)])
+def test_pair_stream_k_tail(G, cm, cn, ma, mb):
+    p = Problem(1024, 1536, 1152, la="row", lb="row", out="bf16", beta=0.5, seed=18)
+    got = _run(G, p, 1.0, 0.5, cta_group=2, cluster_m=cm, cluster_n=cn, mode="mcast", mcast_a=ma, mcast_b=mb,
+               schedule="stream_k", max_clusters=5)
+    assert_close(got, p.reference(1.0, 0.5), 1152, "bf16", f"pair stream-K {cm}x{cn}")
