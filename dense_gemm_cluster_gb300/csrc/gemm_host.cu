@@ -73,8 +73,9 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
         return fail(err, GEMM_ERR_UNSUPPORTED, "block_k must be 0, 64 or 128");
     if (o.group_m < 0 || o.max_clusters < 0 || o.stages < 0)
         return fail(err, GEMM_ERR_INVALID_ARG, "group_m, max_clusters and stages must be >= 0");
-    if (o.schedule < 0 || o.schedule > 2)
-        return fail(err, GEMM_ERR_INVALID_ARG, "schedule must be 0 (auto), 1 (whole tiles) or 2 (stream-K tail)");
+    if (o.schedule < 0 || o.schedule > 3)
+        return fail(err, GEMM_ERR_INVALID_ARG,
+                    "schedule must be 0 (auto), 1 (whole tiles), 2 (stream-K tail) or 3 (cluster launch control)");
     if (M < 0 || N < 0 || K < 0 || batch < 0)
         return fail(err, GEMM_ERR_INVALID_ARG, "negative size");
     if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) || batch >= (1ll << 31))
@@ -99,7 +100,7 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     // 1024 for aligning the dynamic base, the epilogue staging, then per stage a
     // full and an empty barrier, plus 5 barriers, the TMEM address, the abort flag
     // and the epilogue warps' agreement words.
-    const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 5 * 8 + 32;
+    const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 5 * 8 + 32 + 256;   // + the tile-id ring
     auto stage_bytes_for = [&](int bk) { return dgc::BLOCK_M * bk * 2 + (BN / G) * bk * 2; };
     // Operands as launched (after the C^T transpose): K-major ones need K % 64 == 0
     // for the k-split map that 128-wide stages use.
@@ -163,7 +164,7 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
 // co-resident clusters. Returns the number of tiles processed whole (a multiple
 // of `clusters`); the rest are split by k-blocks.
 int64_t whole_tiles_for(int schedule, int64_t tiles, int64_t clusters, int num_kb, bool can_split) {
-    if (!can_split || schedule == 1 || num_kb < 2 || tiles == 0 || clusters <= 1) return tiles;
+    if (!can_split || schedule == 1 || schedule == 3 || num_kb < 2 || tiles == 0 || clusters <= 1) return tiles;
     const int64_t waves = (tiles + clusters - 1) / clusters;
     const double fill = (double)tiles / (double)(waves * clusters);
     if (schedule == 0 && fill >= 0.9) return tiles;
@@ -563,6 +564,11 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
         occ = n;
     }
     int64_t clusters = pl.clusters < occ ? pl.clusters : occ;
+    if (o.schedule == 3) {
+        // One cluster per tile; the resident ones take the pending ones' tiles.
+        clusters = pl.tiles;
+        kp.clc = 1;
+    }
     cfg.gridDim = dim3((unsigned)(clusters * cs), 1, 1);
     // Stream-K tail (needs the co-residency the occupancy cap guarantees, and a workspace).
     if (o.schedule == 2 && h->no_alloc)

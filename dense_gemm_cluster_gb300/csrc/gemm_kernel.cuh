@@ -64,7 +64,11 @@ enum : uint32_t {
     ERR_WAIT_TMEM_FULL = 4,  // epilogue waiting for an accumulator
     ERR_WAIT_DRAIN = 5,      // teardown waiting for in-flight MMAs
     ERR_WAIT_PARTIAL = 6,    // stream-K finisher waiting for another cluster's partial
+    ERR_WAIT_TILE_ID = 7,    // a role waiting for the next tile from cluster launch control
+    ERR_WAIT_TILE_SLOT = 8,  // the scheduler waiting for a free tile-id slot
 };
+
+constexpr int TILE_RING = 4;   // cluster-launch-control responses in flight per cluster
 
 struct KernelParams {
     int M, N, K;             // problem (after any transpose for column-major C)
@@ -92,6 +96,7 @@ struct KernelParams {
     float* workspace;        // one BLOCK_M x BN fp32 partial slot per CTA of the grid
     unsigned int* flags;     // per slot: the epoch whose partial the slot holds
     unsigned int epoch;      // this launch's epoch (never 0)
+    int clc;                 // 1: one cluster per tile; running clusters take pending ones' tiles
 };
 
 struct TileCoord {
@@ -129,6 +134,25 @@ struct Work {
     int contrib_first, contrib_count;   // FINISHER: clusters whose slots hold the rest
 };
 
+// Cluster launch control ("Clusters, distributed shared memory & cluster launch
+// control", sections "Cluster launch control" and "The work-stealing loop"):
+// the grid has one cluster per tile; a running cluster asks the hardware to
+// cancel a not-yet-launched cluster and takes its tile. The request for the
+// next tile goes out before the current tile is computed; the loop ends when a
+// request comes back not canceled (there is no sentinel tile id). Responses
+// land in a small ring in every CTA of the cluster; every role reads them.
+struct ClcCtx {
+    uint32_t resp0;          // shared address of response slot 0 (16 bytes each)
+    uint32_t full0;          // ring "response landed" barriers (8 bytes each)
+    uint32_t empty_rank0;    // rank 0's ring "slot read by everyone" barrier 0, as a cluster address
+    uint32_t cs;             // CTAs per cluster
+    volatile int* abort_flag;
+    int consumed;            // ring entries read so far
+    bool arrive;             // this thread reports its reads (one thread per role)
+};
+
+__device__ bool clc_next(const KernelParams& p, ClcCtx& c, long long& tile);
+
 // Static persistent schedule with a stream-K tail ("Clusters, distributed
 // shared memory & cluster launch control", section "The second wall": a fixed
 // stride leaves SMs idle in the last wave when tiles do not divide evenly;
@@ -136,8 +160,12 @@ struct Work {
 // every CTA of a cluster walks the same sequence.
 struct WorkIter {
     long long dp_next, sk_it, sk_end, cid, ncl, base, rem;
+    ClcCtx* clc = nullptr;   // set: tiles come from cluster launch control
+    bool first_done = false;
 
-    __device__ void init(const KernelParams& p, long long cluster, long long clusters) {
+    __device__ void init(const KernelParams& p, long long cluster, long long clusters, ClcCtx* ctx = nullptr) {
+        clc = p.clc ? ctx : nullptr;
+        first_done = false;
         cid = cluster;
         ncl = clusters;
         dp_next = cluster;
@@ -149,6 +177,16 @@ struct WorkIter {
     __device__ long long start_of(long long c) const { return c * base + (c < rem ? c : rem); }
 
     __device__ bool next(const KernelParams& p, Work& w) {
+        if (clc) {
+            long long t = cid;                  // the first tile is this cluster's own
+            if (first_done && !clc_next(p, *clc, t)) return false;
+            first_done = true;
+            w.tile = t;
+            w.kb0 = 0;
+            w.kb1 = p.num_kb;
+            w.kind = WORK_WHOLE;
+            return true;
+        }
         if (dp_next < p.dp_tiles) {
             w.tile = dp_next;
             w.kb0 = 0;
@@ -220,6 +258,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     }
 }
 
+// Reads the next cluster-launch-control response: false when the request was
+// not canceled (no tile left) or the wait ran out.
+__device__ bool clc_next(const KernelParams& p, ClcCtx& c, long long& tile) {
+    const int slot = c.consumed % TILE_RING;
+    const uint32_t phase = (uint32_t)(c.consumed / TILE_RING) & 1u;
+    if (!wait_bounded(c.full0 + 8u * slot, phase, p, c.abort_flag, ERR_WAIT_TILE_ID, (uint32_t)slot, -1))
+        return false;
+    uint32_t x = 0;
+    const bool got = clc_decode(c.resp0 + 16u * slot, &x);
+    if (c.arrive) mbar_arrive_cluster(c.empty_rank0 + 8u * slot);
+    ++c.consumed;
+    if (!got) return false;
+    tile = (long long)(x / c.cs);
+    return true;
+}
+
 // Bitmask of the CTAs of cluster row `rx` (same A rows), ranks rx + cx*y.
 __device__ __forceinline__ uint32_t row_mask(int rx, int cx, int cy) {
     uint32_t m = 0;
@@ -284,7 +338,8 @@ template <int G, int BK>
 __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan& op, bool is_a, uint32_t full0,
                                         uint32_t empty0, uint32_t rank, uint32_t leader, int cx, int cy, int rx,
                                         int ry, int BNv, int BN_CTAv, volatile int* abort_flag,
-                                        long long cluster, long long clusters, int S) {
+                                        long long cluster, long long clusters, int S, ClcCtx* clc,
+                                        uint32_t ring_empty0) {
     constexpr int NAT = BK / ATOM_K;             // swizzle atoms per stage along K
     // Arm targets: the barrier that counts each receiver's bytes (the receiver
     // itself, or its pair's even CTA), resolved once and indexed by receiver
@@ -319,10 +374,24 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     int stage = 0;
     uint32_t phase = 0;
     WorkIter wi;
-    wi.init(p, cluster, clusters);
+    wi.init(p, cluster, clusters, clc);
     Work w;
+    const bool scheduler = p.clc && is_a && rank == 0;
+    int requests = 0;
     while (wi.next(p, w)) {
         const long long t = w.tile;
+        if (scheduler) {
+            // Ask for the next tile before computing this one.
+            const int slot = requests % TILE_RING;
+            const uint32_t ph = (uint32_t)(requests / TILE_RING) & 1u;
+            if (!wait_bounded<true>(ring_empty0 + 8u * slot, ph ^ 1u, p, abort_flag, ERR_WAIT_TILE_SLOT,
+                                    (uint32_t)slot, t))
+                return false;
+            for (uint32_t r = 0; r < clc->cs; ++r)
+                mbar_arrive_expect_tx_cluster(mapa(clc->full0 + 8u * slot, r), 16u);
+            clc_try_cancel(clc->resp0 + 16u * slot, clc->full0 + 8u * slot, clc->cs > 1);
+            ++requests;
+        }
         const TileCoord tc = tile_coord(p, t);
         const int mn0 = is_a ? (tc.ctm * cx + rx) * BLOCK_M
                              : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
@@ -391,6 +460,10 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // 4 entries, one per epilogue warp
+    uint8_t* ring = reinterpret_cast<uint8_t*>(((reinterpret_cast<uintptr_t>(tmem_slot + 6)) + 15) & ~uintptr_t(15));
+    const uint32_t ring_resp0 = smem_u32(ring);                                // TILE_RING x 16 bytes
+    uint64_t* ring_full = reinterpret_cast<uint64_t*>(ring + 16 * TILE_RING);
+    uint64_t* ring_empty = ring_full + TILE_RING;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -418,6 +491,11 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(smem_u32(&tempty_bar[i]), (uint32_t)(G * EPI_WARPS));
         }
         mbar_init(smem_u32(drain_bar), 1);
+        for (int i = 0; i < TILE_RING; ++i) {
+            mbar_init(smem_u32(&ring_full[i]), 1);
+            // every CTA's two producers, MMA thread and four epilogue warps read each response
+            mbar_init(smem_u32(&ring_empty[i]), (uint32_t)(7 * cx * cy));
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -433,6 +511,14 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     const long long cluster = cluster_id_x();
     const long long clusters = num_clusters_x();
+    ClcCtx clc_ctx;
+    clc_ctx.resp0 = ring_resp0;
+    clc_ctx.full0 = smem_u32(&ring_full[0]);
+    clc_ctx.empty_rank0 = mapa(smem_u32(&ring_empty[0]), 0);
+    clc_ctx.cs = (uint32_t)(cx * cy);
+    clc_ctx.abort_flag = abort_flag;
+    clc_ctx.consumed = 0;
+    clc_ctx.arrive = true;
 
     if (warp == 0 || warp == 6) {
         // ------------------------------------------------------------ producers (A: warp 0, B: warp 6)
@@ -447,7 +533,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB};
             }
             produce<G, BK>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
-                       BN, BN_CTA, abort_flag, cluster, clusters, S);
+                       BN, BN_CTA, abort_flag, cluster, clusters, S, &clc_ctx, smem_u32(&ring_empty[0]));
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -482,7 +568,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t local_tile = 0;
             bool ok = true;
             WorkIter wi;
-            wi.init(p, cluster, clusters);
+            wi.init(p, cluster, clusters, &clc_ctx);
             Work w;
             for (; ok && wi.next(p, w); ++local_tile) {
                 const long long t = w.tile;
@@ -517,6 +603,13 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 mma_commit<G>(smem_u32(drain_bar));
                 wait_bounded(smem_u32(drain_bar), 0, p, abort_flag, ERR_WAIT_DRAIN, 0, -1);
             }
+        } else if (lane == 0 && p.clc) {
+            // The pair's odd CTA issues no MMA but still reads every tile id.
+            WorkIter wi;
+            wi.init(p, cluster, clusters, &clc_ctx);
+            Work w;
+            while (wi.next(p, w)) {
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -532,15 +625,18 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const long long slot = cluster * cs + rank;       // this CTA's stream-K workspace slot
         uint32_t local_tile = 0;
         uint32_t buf = 0;
+        ClcCtx epi_clc = clc_ctx;
+        epi_clc.arrive = lane == 0;
         WorkIter wi;
-        wi.init(p, cluster, clusters);
+        wi.init(p, cluster, clusters, &epi_clc);
         Work w;
-        for (; wi.next(p, w); ++local_tile) {
+        for (;; ++local_tile) {
+            const bool have = wi.next(p, w);
             const long long t = w.tile;
             const uint32_t acc = local_tile & 1u;
             const uint32_t acc_phase = (local_tile >> 1) & 1u;
-            const bool ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, p, abort_flag,
-                                         ERR_WAIT_TMEM_FULL, acc, t);
+            const bool ok = have && wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, p, abort_flag,
+                                                 ERR_WAIT_TMEM_FULL, acc, t);
             // The four epilogue warps agree on going on, so that none is ever left
             // alone at the named barrier below after another has stopped.
             if (lane == 0) epi_ok[ew] = ok ? 1 : 0;

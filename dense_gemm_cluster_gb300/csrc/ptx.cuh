@@ -114,6 +114,35 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Ask the hardware to cancel one not-yet-launched cluster of this grid; the
+// 16-byte response lands in `resp` of every CTA of this cluster (or this CTA
+// only) and completes 16 transaction bytes on `bar` at the same offset.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar, bool whole_cluster) {
+    if (whole_cluster)
+        asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+                     ".multicast::cluster::all.b128 [%0], [%1];" :: "r"(resp), "r"(bar) : "memory");
+    else
+        asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+                     :: "r"(resp), "r"(bar) : "memory");
+}
+// Decodes a response: true if a cluster was canceled (its first CTA's x index
+// goes to *ctaid_x); false means no launch was left to take, and *ctaid_x is
+// not meaningful.
+__device__ __forceinline__ bool clc_decode(uint32_t resp, uint32_t* ctaid_x) {
+    uint32_t ok, x, y, z, w;
+    asm volatile(
+        "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 h, [%5];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, %2, %3, %4}, h;\n\t}"
+        : "=r"(ok), "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "r"(resp) : "memory");
+    (void)y; (void)z; (void)w;
+    *ctaid_x = x;
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- global flags
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
     unsigned int v;

@@ -185,7 +185,7 @@ def make_options(**kw) -> gemm_options_t:
     out_type as "bf16"/"f32", mode as "unicast"/"mcast")."""
     o = gemm_options_default()
     names = {"row": GEMM_ROW_MAJOR, "col": GEMM_COL_MAJOR, "bf16": GEMM_OUT_BF16, "f32": GEMM_OUT_F32,
-             "unicast": GEMM_MODE_UNICAST, "mcast": GEMM_MODE_MCAST, "auto": 0, "dp": 1, "stream_k": 2}
+             "unicast": GEMM_MODE_UNICAST, "mcast": GEMM_MODE_MCAST, "auto": 0, "dp": 1, "stream_k": 2, "clc": 3}
     for k, v in kw.items():
         if not hasattr(o, k):
             raise TypeError(f"gemm_options_t has no field {k!r}")

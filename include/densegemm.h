@@ -87,7 +87,10 @@ typedef struct {
     int stages;         /* shared-memory pipeline depth; 0 = as many as fit */
     int max_clusters;   /* cap on the persistent grid, in clusters; 0 = as many as are co-resident */
     int group_m;        /* raster band height, in cluster tiles along M; 0 = 8 */
-    int schedule;       /* 0 = auto, 1 = whole tiles only, 2 = stream-K tail: the tiles
+    int schedule;       /* 0 = auto, 1 = whole tiles only, 3 = cluster launch control (one
+                           cluster per tile; running clusters cancel pending launches and take
+                           their tiles, asking for the next tile before computing the current
+                           one), 2 = stream-K tail: the tiles
                            left after the last full wave (between one and two waves'
                            worth) are split by k-blocks evenly over all clusters, and the
                            parts are summed in a fixed order. Auto uses it when whole tiles

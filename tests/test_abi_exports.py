@@ -143,4 +143,6 @@ def test_plan_stream_k_tail(lib):
     assert p.stream_k_tiles == 0
     s, p = plan(lib, 4096, 4096, 64, sm=152)
     assert p.stream_k_tiles == 0
-    assert plan(lib, 64, 64, 64, schedule=3)[0] == 1
+    assert plan(lib, 64, 64, 64, schedule=4)[0] == 1
+    s, p = plan(lib, 4096, 4096, 4096, sm=152, schedule="clc")
+    assert s == 0 and p.stream_k_tiles == 0
