@@ -59,6 +59,8 @@ def _load():
             lib.oracle_gemm_entries.restype = i32
             lib.oracle_attention_scores.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp]
             lib.oracle_attention_scores.restype = i32
+            lib.oracle_stencil_1d.argtypes = [i64, vp, vp]
+            lib.oracle_stencil_1d.restype = i32
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -133,3 +135,13 @@ def attention_scores(Q, Kmat):
     if rc != 0:
         raise ValueError(f"oracle_attention_scores rejected its arguments (code {rc})")
     return out
+
+
+def stencil_1d(x):
+    """y[i] = 0.25 x[i-1] + 0.5 x[i] + 0.25 x[i+1] (x = 0 outside the array), float64 out."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape[0], dtype=np.float64)
+    rc = _load().oracle_stencil_1d(x.shape[0], _ptr(x), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"oracle_stencil_1d rejected its arguments (code {rc})")
+    return y

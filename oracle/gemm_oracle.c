@@ -143,3 +143,21 @@ int oracle_num_threads(void)
 {
     return omp_get_max_threads();
 }
+
+/*
+ * 1-D three-point stencil of the cluster halo-exchange example ("集群编程",
+ * section 实践示例：Halo 交换): y[i] = 0.25*x[i-1] + 0.5*x[i] + 0.25*x[i+1],
+ * float32 inputs widened to double, x taken as 0 outside [0, n).
+ */
+int oracle_stencil_1d(int64_t n, const float *x, double *y)
+{
+    if (n < 0)
+        return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const double l = i > 0 ? (double)x[i - 1] : 0.0;
+        const double r = i + 1 < n ? (double)x[i + 1] : 0.0;
+        y[i] = 0.25 * l + 0.5 * (double)x[i] + 0.25 * r;
+    }
+    return 0;
+}

@@ -235,3 +235,36 @@ def test_empty_shapes():
     assert oracle.gemm(0, 8, 8, A, 8, "row", B, 8, "row").shape == (0, 8)
     z = oracle.gemm(3, 4, 0, np.zeros((3, 8), np.uint16), 8, "row", np.zeros((0, 8), np.uint16), 8, "row")
     assert np.array_equal(z, np.zeros((3, 4)))
+
+
+# ---------------------------------------------------------------- 1-D stencil pins
+def test_stencil_constant_and_linear_interiors_are_exact():
+    c = np.full(50, 3.5, dtype=np.float32)
+    y = oracle.stencil_1d(c)
+    assert np.array_equal(y[1:-1], np.full(48, 3.5))
+    assert y[0] == y[-1] == 0.75 * 3.5                 # one neighbour is outside: counts as zero
+    lin = np.arange(40, dtype=np.float32)
+    y = oracle.stencil_1d(lin)
+    assert np.array_equal(y[1:-1], np.arange(1, 39, dtype=np.float64))   # a linear ramp is reproduced
+    assert y[-1] == 0.25 * 38 + 0.5 * 39
+
+
+def test_stencil_impulse_response_is_quarter_half_quarter():
+    x = np.zeros(9, dtype=np.float32)
+    x[4] = 8.0
+    assert list(oracle.stencil_1d(x)) == [0, 0, 0, 2.0, 4.0, 2.0, 0, 0, 0]
+    x = np.zeros(5, dtype=np.float32)
+    x[0] = 4.0                                          # at the edge only one side spreads
+    assert list(oracle.stencil_1d(x)) == [2.0, 1.0, 0, 0, 0]
+
+
+def test_stencil_is_linear_and_symmetric():
+    rng = np.random.default_rng(5)
+    a = rng.standard_normal(33).astype(np.float32)
+    b = rng.standard_normal(33).astype(np.float32)
+    lhs = oracle.stencil_1d(a) + oracle.stencil_1d(b)
+    rhs = oracle.stencil_1d((a.astype(np.float64) + b).astype(np.float32))
+    assert np.allclose(lhs, rhs, atol=1e-6)
+    assert np.array_equal(oracle.stencil_1d(a[::-1].copy())[::-1], oracle.stencil_1d(a))  # mirror symmetry
+    assert oracle.stencil_1d(np.zeros(0, np.float32)).shape == (0,)
+    assert oracle.stencil_1d(np.array([2.0], np.float32))[0] == 1.0
