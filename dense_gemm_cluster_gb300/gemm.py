@@ -274,3 +274,19 @@ def tma_bench_query_status(stream=None) -> int:
 
 def tma_bench_last_error() -> str:
     return (_lib.tma_bench_last_error() or b"").decode()
+
+
+# ---------------------------------------------------------------- cluster halo-exchange stencil (include/stencil.h)
+STENCIL_TILE = 8192
+_lib.stencil_1d_run.argtypes = [_vp, _vp, _i64, _i32, _vp]
+_lib.stencil_1d_run.restype = _i32
+_lib.stencil_1d_query_status.argtypes = [_vp]
+_lib.stencil_1d_query_status.restype = _i32
+
+
+def stencil_1d_run(x, y, n, cluster, stream=None) -> int:
+    return _lib.stencil_1d_run(_ptr(x), _ptr(y), n, cluster, _stream(stream))
+
+
+def stencil_1d_query_status(stream=None) -> int:
+    return _lib.stencil_1d_query_status(_stream(stream))
