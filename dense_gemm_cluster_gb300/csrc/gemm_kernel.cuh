@@ -433,6 +433,142 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     return true;
 }
 
+// One epilogue warp's rows of one output tile.
+struct EpiTile {
+    uint32_t t_row;      // TMEM address of this warp's lanes, this accumulator's column 0
+    int n0;              // first column of the tile
+    int row0;            // first global row this warp stores (32 rows)
+    int row;             // the row this thread stores
+    int trow;            // that row within the tile
+    int b;               // batch
+    int lane;
+    uint32_t tempty;     // barrier to hand the accumulator back on (cluster address)
+    int contrib_first, contrib_count, cs, rank;   // stream-K finisher only
+};
+
+// TMEM -> registers -> (stream-K partials) -> alpha * acc + beta * C_in -> bf16/fp32
+// -> 128-byte-swizzled shared rows -> TMA store, in 128-byte-wide column chunks,
+// double-buffered per warp. Specialised on the output type and on whether
+// partials are added, so whole tiles run the lean loop.
+template <int BN, int G, bool OUT_F32, bool FIXUP>
+__device__ __forceinline__ void store_tile(const KernelParams& p, const CUtensorMap* tmC, const EpiTile& e,
+                                           uint8_t* stage_ptr, uint32_t stage_base, uint32_t& buf) {
+    constexpr int CW = OUT_F32 ? 32 : 64;             // columns per 128-byte store row
+    constexpr int chunks = BN / CW;
+    const bool use_beta = p.beta != 0.0f;
+    for (int c = 0; c < chunks; ++c) {
+        const int col0 = e.n0 + c * CW;
+        float v[CW];
+        {
+            uint32_t r[32];
+            tmem_ld_32cols(e.t_row + c * CW, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        }
+        if (!OUT_F32) {
+            uint32_t r[32];
+            tmem_ld_32cols(e.t_row + c * CW + 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[(CW - 32) + i] = __uint_as_float(r[i]);
+        }
+        if (FIXUP) {
+            // Add the other contributors' partials, in cluster order.
+            for (int i = 0; i < e.contrib_count; ++i) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    p.workspace + (((long long)(e.contrib_first + i) * e.cs + e.rank) * BLOCK_M + e.trow) *
+                                      (long long)BN + c * CW);
+#pragma unroll
+                for (int j = 0; j < CW / 4; ++j) {
+                    const float4 a = src[j];
+                    v[4 * j] += a.x;
+                    v[4 * j + 1] += a.y;
+                    v[4 * j + 2] += a.z;
+                    v[4 * j + 3] += a.w;
+                }
+            }
+        }
+        if (c == chunks - 1) {
+            // All of this accumulator is in registers: hand it back.
+            tc_fence_before();
+            __syncwarp();
+            // CTA-scope release for a CTA's own barrier; cluster scope only when the
+            // pair's odd CTA hands back to the even one.
+            if (e.lane == 0) {
+                if (G == 2) mbar_arrive_cluster(e.tempty);
+                else        mbar_arrive_local(e.tempty);
+            }
+        }
+        // alpha * acc + beta * C_in, in fp32.
+        if (use_beta) {
+            const bool row_ok = e.row < p.M;
+            if (OUT_F32) {
+                const float* src = static_cast<const float*>(p.c_in) + (long long)e.b * p.stride_c +
+                                   (long long)e.row * p.ldc + col0;
+#pragma unroll
+                for (int i = 0; i < CW; ++i) {
+                    const float ci = (row_ok && col0 + i < p.N) ? src[i] : 0.0f;
+                    v[i] = fmaf(p.alpha, v[i], p.beta * ci);
+                }
+            } else {
+                const uint16_t* src = static_cast<const uint16_t*>(p.c_in) + (long long)e.b * p.stride_c +
+                                      (long long)e.row * p.ldc + col0;
+                if (row_ok && col0 + CW <= p.N) {
+                    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+                    for (int j = 0; j < CW / 8; ++j) {
+                        const uint4 q = s4[j];
+                        const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const float lo = __uint_as_float(ws[h] << 16);
+                            const float hi = __uint_as_float(ws[h] & 0xFFFF0000u);
+                            v[8 * j + 2 * h] = fmaf(p.alpha, v[8 * j + 2 * h], p.beta * lo);
+                            v[8 * j + 2 * h + 1] = fmaf(p.alpha, v[8 * j + 2 * h + 1], p.beta * hi);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) {
+                        const float ci = (row_ok && col0 + i < p.N) ? __uint_as_float((uint32_t)src[i] << 16) : 0.0f;
+                        v[i] = fmaf(p.alpha, v[i], p.beta * ci);
+                    }
+                }
+            }
+        } else if (p.alpha != 1.0f) {
+#pragma unroll
+            for (int i = 0; i < CW; ++i) v[i] *= p.alpha;
+        }
+        // Pack one 128-byte row per thread.
+        uint32_t w[32];
+        if (OUT_F32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        }
+        // The buffer about to be written was last used two stores ago.
+        if (e.lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        uint8_t* rowp = stage_ptr + buf * EPI_BUF_BYTES + e.lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
+            uint4* dst = reinterpret_cast<uint4*>(rowp + ((j ^ (e.lane & 7)) << 4));
+            *dst = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (e.lane == 0) {
+            tma_store_3d(tmC, stage_base + buf * EPI_BUF_BYTES, col0, e.row0, e.b);
+            bulk_commit_group();
+        }
+        buf ^= 1u;
+    }
+}
+
 template <int BN, int G, int BK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -459,7 +595,6 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t* drain_bar = bars + 2 * S + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);   // 4 entries, one per epilogue warp
     uint8_t* ring = reinterpret_cast<uint8_t*>(((reinterpret_cast<uintptr_t>(tmem_slot + 6)) + 15) & ~uintptr_t(15));
     const uint32_t ring_resp0 = smem_u32(ring);                                // TILE_RING x 16 bytes
     uint64_t* ring_full = reinterpret_cast<uint64_t*>(ring + 16 * TILE_RING);
@@ -617,33 +752,33 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int ew = warp - 2;                          // staging buffers of this warp
         const uint32_t stage_base = smem_u32(sEpi + ew * 2 * EPI_BUF_BYTES);
         uint8_t* stage_ptr = sEpi + ew * 2 * EPI_BUF_BYTES;
-        const int CW = p.out_f32 ? 32 : 64;               // columns per 128-byte store row
-        const int chunks = BN / CW;
-
-        const bool use_beta = p.beta != 0.0f;
         const int cs = cx * cy;
         const long long slot = cluster * cs + rank;       // this CTA's stream-K workspace slot
         uint32_t local_tile = 0;
         uint32_t buf = 0;
+        // Where this warp hands accumulators back: the pair's even CTA for the pair MMA.
+        const uint32_t tempty_addr = (G == 2) ? mapa(smem_u32(&tempty_bar[0]), leader) : smem_u32(&tempty_bar[0]);
         ClcCtx epi_clc = clc_ctx;
         epi_clc.arrive = lane == 0;
         WorkIter wi;
         wi.init(p, cluster, clusters, &epi_clc);
         Work w;
+        // A warp whose wait fails goes on walking the (deterministic) work list
+        // without doing the work, so it still joins every named barrier the
+        // other epilogue warps reach: none is ever left waiting there alone.
+        bool dead = false;
         for (;; ++local_tile) {
-            const bool have = wi.next(p, w);
+            if (!wi.next(p, w)) break;
             const long long t = w.tile;
             const uint32_t acc = local_tile & 1u;
             const uint32_t acc_phase = (local_tile >> 1) & 1u;
-            const bool ok = have && wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, p, abort_flag,
-                                                 ERR_WAIT_TMEM_FULL, acc, t);
-            // The four epilogue warps agree on going on, so that none is ever left
-            // alone at the named barrier below after another has stopped.
-            if (lane == 0) epi_ok[ew] = ok ? 1 : 0;
-            epilogue_bar();
-            const bool all_ok = epi_ok[0] && epi_ok[1] && epi_ok[2] && epi_ok[3];
-            epilogue_bar();
-            if (!all_ok) break;
+            if (!dead && !wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, p, abort_flag,
+                                       ERR_WAIT_TMEM_FULL, acc, t))
+                dead = true;
+            if (dead) {
+                if (w.kind != WORK_WHOLE) epilogue_bar();
+                continue;
+            }
             tc_fence_after();
             const TileCoord tc = tile_coord(p, t);
             const int m0 = (tc.ctm * cx + rx) * BLOCK_M;
@@ -662,8 +797,8 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
-                            if (G == 2) mbar_arrive_cluster(mapa(smem_u32(&tempty_bar[acc]), leader));
-                            else        mbar_arrive_local(smem_u32(&tempty_bar[acc]));
+                            if (G == 2) mbar_arrive_cluster(tempty_addr + 8u * acc);
+                            else        mbar_arrive_local(tempty_addr + 8u * acc);
                         }
                     }
                     float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
@@ -695,118 +830,14 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 epilogue_bar();
             }
-            for (int c = 0; c < chunks; ++c) {
-                const int col0 = n0 + c * CW;
-                float v[64];
-                {
-                    uint32_t r[32];
-                    tmem_ld_32cols(t_row + c * CW, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                }
-                if (!p.out_f32) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(t_row + c * CW + 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
-                }
-                if (w.kind == WORK_FINISHER) {
-                    // Add the other contributors' partials, in cluster order.
-                    const int nv = p.out_f32 ? 32 : 64;
-                    for (int i = 0; i < w.contrib_count; ++i) {
-                        const float4* src = reinterpret_cast<const float4*>(
-                            p.workspace + (((long long)(w.contrib_first + i) * cs + rank) * BLOCK_M + trow) *
-                                              (long long)BN + c * CW);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (4 * j < nv) {
-                                const float4 a = src[j];
-                                v[4 * j] += a.x;
-                                v[4 * j + 1] += a.y;
-                                v[4 * j + 2] += a.z;
-                                v[4 * j + 3] += a.w;
-                            }
-                        }
-                    }
-                }
-                if (c == chunks - 1) {
-                    // All of this accumulator is in registers: hand it back.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (G == 2) mbar_arrive_cluster(mapa(smem_u32(&tempty_bar[acc]), leader));
-                        else        mbar_arrive_local(smem_u32(&tempty_bar[acc]));
-                    }
-                }
-                // alpha * acc + beta * C_in, in fp32.
-                if (use_beta) {
-                    const bool row_ok = row < p.M;
-                    if (p.out_f32) {
-                        const float* src = static_cast<const float*>(p.c_in) + (long long)tc.b * p.stride_c +
-                                           (long long)row * p.ldc + col0;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float ci = (row_ok && col0 + i < p.N) ? src[i] : 0.0f;
-                            v[i] = fmaf(p.alpha, v[i], p.beta * ci);
-                        }
-                    } else {
-                        const uint16_t* src = static_cast<const uint16_t*>(p.c_in) + (long long)tc.b * p.stride_c +
-                                              (long long)row * p.ldc + col0;
-                        if (row_ok && col0 + 64 <= p.N) {
-                            const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const uint4 w = s4[j];
-                                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    const float lo = __uint_as_float(ws[h] << 16);
-                                    const float hi = __uint_as_float(ws[h] & 0xFFFF0000u);
-                                    v[8 * j + 2 * h] = fmaf(p.alpha, v[8 * j + 2 * h], p.beta * lo);
-                                    v[8 * j + 2 * h + 1] = fmaf(p.alpha, v[8 * j + 2 * h + 1], p.beta * hi);
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 64; ++i) {
-                                const float ci = (row_ok && col0 + i < p.N)
-                                                     ? __uint_as_float((uint32_t)src[i] << 16) : 0.0f;
-                                v[i] = fmaf(p.alpha, v[i], p.beta * ci);
-                            }
-                        }
-                    }
-                } else if (p.alpha != 1.0f) {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) v[i] *= p.alpha;
-                }
-                // Pack one 128-byte row per thread.
-                uint32_t w[32];
-                if (p.out_f32) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                }
-                // The buffer about to be written was last used two stores ago.
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
-                uint8_t* rowp = stage_ptr + buf * EPI_BUF_BYTES + lane * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
-                    uint4* dst = reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4));
-                    *dst = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&tmC, stage_base + buf * EPI_BUF_BYTES, col0, m0 + q * 32, tc.b);
-                    bulk_commit_group();
-                }
-                buf ^= 1u;
+            const EpiTile et{t_row, n0, m0 + q * 32, row, trow, tc.b, lane, tempty_addr + 8u * acc,
+                             w.contrib_first, w.contrib_count, cs, (int)rank};
+            if (p.out_f32) {
+                if (w.kind == WORK_FINISHER) store_tile<BN, G, true, true>(p, &tmC, et, stage_ptr, stage_base, buf);
+                else                         store_tile<BN, G, true, false>(p, &tmC, et, stage_ptr, stage_base, buf);
+            } else {
+                if (w.kind == WORK_FINISHER) store_tile<BN, G, false, true>(p, &tmC, et, stage_ptr, stage_base, buf);
+                else                         store_tile<BN, G, false, false>(p, &tmC, et, stage_ptr, stage_base, buf);
             }
         }
         if (lane == 0) bulk_wait_group<0>();

@@ -130,7 +130,8 @@ __device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar, bool
 // goes to *ctaid_x); false means no launch was left to take, and *ctaid_x is
 // not meaningful.
 __device__ __forceinline__ bool clc_decode(uint32_t resp, uint32_t* ctaid_x) {
-    uint32_t ok, x, y, z, w;
+    uint32_t ok, x;
+    uint32_t y, z, w;   // the other coordinates of the first CTA (1-D grids use x only)
     asm volatile(
         "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
         "ld.shared.b128 h, [%5];\n\t"
@@ -138,8 +139,7 @@ __device__ __forceinline__ bool clc_decode(uint32_t resp, uint32_t* ctaid_x) {
         "selp.u32 %0, 1, 0, p;\n\t"
         "clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, %2, %3, %4}, h;\n\t}"
         : "=r"(ok), "=r"(x), "=r"(y), "=r"(z), "=r"(w) : "r"(resp) : "memory");
-    (void)y; (void)z; (void)w;
-    *ctaid_x = x;
+    *ctaid_x = x + 0u * (y | z | w);
     return ok != 0;
 }
 
