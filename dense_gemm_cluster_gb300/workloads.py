@@ -63,6 +63,12 @@ WORKLOADS = {
         options=dict(mode="mcast", mcast_b=1, cluster_m=4, cluster_n=1, cta_group=2, block_n=256),
         description="GEMM 8192^3, N(0,1)/sqrt(K), bf16 out, beta=0.5 with bf16 C ~ N(0,1), "
                     "cta_group::2 256x256 tiles, 4-CTA cluster multicasting B"),
+    "gemm8192_bf16_unicast": Workload(
+        "gemm8192_bf16_unicast", 8192, 8192, 8192, dist="normal", scale=1.0 / math.sqrt(8192),
+        out="bf16", beta=0.5,
+        options=dict(mode="unicast", cluster_m=1, cluster_n=1, cta_group=1, block_n=256),
+        description="the 8192^3 GEMM above with unicast loads and single-CTA 128x256 tiles (the baseline "
+                    "for the L2->SM operand-byte comparison)"),
     "scores_8x16x4096x4096x128": Workload(
         "scores_8x16x4096x4096x128", 4096, 4096, 128, batch=128, dist="normal", layout_a="row",
         layout_b="col", out="f32",
