@@ -1,0 +1,87 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+The oracle computes sampled outputs one by one (corners, tile edges, random
+interior points); every output is also checked to be finite and of the size
+the input distributions predict. The tolerance is the one the workloads state.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from gpu_cases import BF16_NAN, decode, from_dev, sample_positions, tolerance, torch_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _workload(name):
+    from dense_gemm_cluster_gb300.workloads import WORKLOADS
+    return WORKLOADS[name]
+
+
+def _gemm_for(w):
+    from dense_gemm_cluster_gb300 import gemm
+    return gemm.Gemm(0, layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out, **w.options)
+
+
+def _check_sampled(got_vals, ref_vals, K, out, what):
+    scale = float(np.max(np.abs(ref_vals)))
+    err = float(np.max(np.abs(got_vals - ref_vals))) / scale
+    assert err <= tolerance(K, out), f"{what}: sampled max|err|/max|ref| = {err:.3e}"
+
+
+@pytest.mark.parametrize("name", ["gemm8192_bf16_pair_mcastB4", "skinny_16384x128x8192", "skinny_128x16384x8192"])
+def test_gemm_workload_full_size_sampled(name):
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    w = _workload(name)
+    A_log = inputs.bf16_matrix(w.M, w.K, w.dist, inputs.STREAM_A, w.scale)
+    B_log = inputs.bf16_matrix(w.K, w.N, w.dist, inputs.STREAM_B, w.scale)
+    A, lda = inputs.store(A_log, w.layout_a)
+    B, ldb = inputs.store(B_log, w.layout_b)
+    del A_log, B_log
+    if w.beta != 0.0:
+        C_in, ldc = inputs.store(inputs.bf16_matrix(w.M, w.N, w.c_dist, inputs.STREAM_C), w.layout_c)
+    else:
+        C_in, ldc = inputs.store(np.full((w.M, w.N), BF16_NAN, np.uint16), w.layout_c)
+    g = _gemm_for(w)
+    dC = torch_dev(C_in)
+    g.run(w.M, w.N, w.K, torch_dev(A), lda, torch_dev(B), ldb, dC, ldc, w.alpha, w.beta)
+    assert g.query_status() == 0
+    g.close()
+    got = decode(from_dev(dC, np.uint16), w.M, w.N, w.layout_c)
+    rows, cols = sample_positions(w.M, w.N, 2000, seed=1)
+    ref = oracle.gemm_entries(rows, cols, w.K, A, lda, w.layout_a, B, ldb, w.layout_b, w.alpha, w.beta,
+                              C_in if w.beta != 0.0 else None, ldc, w.layout_c)
+    _check_sampled(got[rows, cols], ref, w.K, w.out, name)
+    assert np.isfinite(got).all()
+    # magnitudes: A and B iid with variances va, vb -> sum over K has variance K va vb (+ beta^2 var C)
+    va = {"normal": 1.0, "uniform": 1.0 / 3.0}[w.dist] * w.scale ** 2
+    expect = math.sqrt(w.K * va * va + (w.beta ** 2 if w.beta else 0.0))
+    assert 0.8 < float(np.std(got)) / expect < 1.25
+
+
+def test_scores_workload_full_size_sampled():
+    import torch
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    w = _workload("scores_8x16x4096x4096x128")
+    Q = inputs.bf16_matrix(w.batch * w.M, w.K, w.dist, inputs.STREAM_A)
+    Kt = inputs.bf16_matrix(w.batch * w.N, w.K, w.dist, inputs.STREAM_B)
+    g = _gemm_for(w)
+    dS = torch.empty(w.batch * w.M * w.N, dtype=torch.float32, device="cuda")
+    g.run_strided_batched(w.M, w.N, w.K, torch_dev(Q), w.K, w.M * w.K, torch_dev(Kt), w.K, w.N * w.K, dS, w.N,
+                          w.M * w.N, w.batch)
+    assert g.query_status() == 0
+    g.close()
+    rng = np.random.default_rng(2)
+    for b in sorted(set([0, w.batch - 1] + list(rng.integers(0, w.batch, size=4)))):
+        S = dS[b * w.M * w.N:(b + 1) * w.M * w.N].view(w.M, w.N)
+        rows, cols = sample_positions(w.M, w.N, 400, seed=int(b))
+        got = S[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].cpu().numpy().astype(np.float64)
+        Qb = Q[b * w.M:(b + 1) * w.M]
+        Kb = Kt[b * w.N:(b + 1) * w.N]
+        ref = oracle.gemm_entries(rows, cols, w.K, Qb, w.K, "row", Kb, w.K, "col")
+        _check_sampled(got, ref, w.K, "f32", f"scores batch {b}")
+        assert bool(torch.isfinite(S).all())
+        assert 0.8 < float(S.std()) / math.sqrt(w.K) < 1.25
