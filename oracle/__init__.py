@@ -39,7 +39,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
         cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-               "-std=c11", _SRC, "-o", tmp]
+               "-std=c11", _SRC, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -59,6 +59,8 @@ def _load():
             lib.oracle_gemm_entries.restype = i32
             lib.oracle_attention_scores.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp]
             lib.oracle_attention_scores.restype = i32
+            lib.oracle_attention_forward.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp, f64, vp, vp]
+            lib.oracle_attention_forward.restype = i32
             lib.oracle_stencil_1d.argtypes = [i64, vp, vp]
             lib.oracle_stencil_1d.restype = i32
             lib.oracle_num_threads.argtypes = []
@@ -145,3 +147,24 @@ def stencil_1d(x):
     if rc != 0:
         raise ValueError(f"oracle_stencil_1d rejected its arguments (code {rc})")
     return y
+
+
+def attention_forward(Q, Kmat, V, scale=None, with_lse=False):
+    """O = softmax(scale Q K^T) V per batch for bf16-bit arrays Q (b, sq, d), K (b, sk, d),
+    V (b, sk, dv); float64 out (and the row log-sum-exp when with_lse). scale defaults to 1/sqrt(d)."""
+    Q = np.ascontiguousarray(Q, dtype=np.uint16)
+    Kmat = np.ascontiguousarray(Kmat, dtype=np.uint16)
+    V = np.ascontiguousarray(V, dtype=np.uint16)
+    b, sq, d = Q.shape
+    sk, dv = V.shape[1], V.shape[2]
+    if Kmat.shape != (b, sk, d) or V.shape[0] != b:
+        raise ValueError("Q, K, V disagree on batch, key count or head dimension")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    O = np.empty((b, sq, dv), dtype=np.float64)
+    lse = np.empty((b, sq), dtype=np.float64)
+    rc = _load().oracle_attention_forward(b, sq, sk, d, dv, _ptr(Q), _ptr(Kmat), _ptr(V), float(scale),
+                                          _ptr(O), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_forward rejected its arguments (code {rc})")
+    return (O, lse) if with_lse else O

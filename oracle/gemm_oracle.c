@@ -25,6 +25,8 @@
 #include <stdint.h>
 #include <string.h>
 #include <omp.h>
+#include <math.h>
+#include <stdlib.h>
 
 /* Exact widening of a bf16 bit pattern: it is the top half of a float32. */
 static double bf16_to_double(uint16_t bits)
@@ -158,6 +160,58 @@ int oracle_stencil_1d(int64_t n, const float *x, double *y)
         const double l = i > 0 ? (double)x[i - 1] : 0.0;
         const double r = i + 1 < n ? (double)x[i + 1] : 0.0;
         y[i] = 0.25 * l + 0.5 * (double)x[i] + 0.25 * r;
+    }
+    return 0;
+}
+
+/*
+ * Attention forward: O = softmax(scale * Q K^T) V per (batch, head), the fused
+ * form of the score product above ("Hopper TMA Multicast 深度解析与实测",
+ * section 经典应用场景: FlashAttention-type operators whose Q-tile CTAs share
+ * the K/V tiles). Plain definition per query row i:
+ *   s_j = scale * sum_t Q[i][t] K[j][t];  m = max_j s_j;  p_j = exp(s_j - m);
+ *   l = sum_j p_j;  O[i] = sum_j p_j V[j] / l;  lse[i] = m + log(l)
+ * (subtracting m leaves the softmax unchanged). Q is batch x sq x d, K is
+ * batch x sk x d, V is batch x sk x dv, all bf16 bits, row-major and dense;
+ * O is batch x sq x dv and lse batch x sq, in double. lse may be NULL.
+ */
+int oracle_attention_forward(int64_t batch, int64_t sq, int64_t sk, int64_t d, int64_t dv,
+                             const uint16_t *Q, const uint16_t *Kmat, const uint16_t *V,
+                             double scale, double *O, double *lse)
+{
+    if (batch < 0 || sq < 0 || sk < 1 || d < 0 || dv < 0)
+        return 1;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t i = 0; i < sq; ++i) {
+            const uint16_t *q = Q + (b * sq + i) * d;
+            double *o = O + (b * sq + i) * dv;
+            double *s = (double *)malloc(sizeof(double) * (size_t)sk);
+            double m = -HUGE_VAL;
+            for (int64_t j = 0; j < sk; ++j) {
+                const uint16_t *kr = Kmat + (b * sk + j) * d;
+                double acc = 0.0;
+                for (int64_t t = 0; t < d; ++t)
+                    acc += bf16_to_double(q[t]) * bf16_to_double(kr[t]);
+                s[j] = scale * acc;
+                if (s[j] > m)
+                    m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < sk; ++j) {
+                s[j] = exp(s[j] - m);
+                l += s[j];
+            }
+            for (int64_t c = 0; c < dv; ++c) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < sk; ++j)
+                    acc += s[j] * bf16_to_double(V[(b * sk + j) * dv + c]);
+                o[c] = acc / l;
+            }
+            if (lse)
+                lse[b * sq + i] = m + log(l);
+            free(s);
+        }
     }
     return 0;
 }

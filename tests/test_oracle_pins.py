@@ -268,3 +268,65 @@ def test_stencil_is_linear_and_symmetric():
     assert np.array_equal(oracle.stencil_1d(a[::-1].copy())[::-1], oracle.stencil_1d(a))  # mirror symmetry
     assert oracle.stencil_1d(np.zeros(0, np.float32)).shape == (0,)
     assert oracle.stencil_1d(np.array([2.0], np.float32))[0] == 1.0
+
+
+# ---------------------------------------------------------------- attention forward pins
+def _attn_inputs(b, sq, sk, d, dv, seed):
+    Q = np.stack([bf16(sq, d, seed=seed + 3 * i) for i in range(b)])
+    K = np.stack([bf16(sk, d, seed=seed + 3 * i + 1) for i in range(b)])
+    V = np.stack([bf16(sk, dv, seed=seed + 3 * i + 2) for i in range(b)])
+    return Q, K, V
+
+
+def test_attention_zero_queries_average_the_values():
+    _, K, V = _attn_inputs(2, 5, 37, 16, 8, 500)
+    Q = np.zeros((2, 5, 16), np.uint16)
+    O, lse = oracle.attention_forward(Q, K, V, with_lse=True)
+    for b in range(2):
+        means = np.array([math.fsum(col) / 37 for col in val(V[b]).T])
+        assert np.allclose(O[b], means[None, :], rtol=0, atol=1e-15)
+        assert np.allclose(lse[b], math.log(37.0), rtol=0, atol=1e-15)     # all scores 0
+
+
+def test_attention_rows_are_convex_combinations():
+    Q, K, _ = _attn_inputs(1, 9, 50, 32, 4, 510)
+    ones = np.full((1, 50, 4), 0x3F80, np.uint16)                         # V = 1
+    assert np.allclose(oracle.attention_forward(Q, K, ones), 1.0, rtol=0, atol=1e-14)
+
+
+def test_attention_dominant_key_selects_its_value():
+    # keys are scaled one-hots; with a large scale the matching key takes all the weight
+    d, sk = 8, 8
+    K = inputs.f64_to_bf16_bits(np.eye(sk, d))[None]
+    Q = inputs.f64_to_bf16_bits(np.eye(sk, d)[[3, 6, 0]])[None]
+    V = bf16(sk, 5, seed=520)[None]
+    O = oracle.attention_forward(Q, K, V, scale=80.0)
+    for r, j in enumerate([3, 6, 0]):
+        assert np.allclose(O[0, r], val(V[0])[j], rtol=0, atol=1e-30)
+
+
+def test_attention_is_invariant_to_key_order_and_keeps_batches_apart():
+    Q, K, V = _attn_inputs(2, 6, 23, 16, 12, 530)
+    perm = np.random.default_rng(1).permutation(23)
+    O = oracle.attention_forward(Q, K, V)
+    assert np.allclose(O, oracle.attention_forward(Q, K[:, perm], V[:, perm]), rtol=0, atol=1e-14)
+    O2 = oracle.attention_forward(Q, K[::-1].copy(), V[::-1].copy())
+    assert not np.allclose(O2[0], O[0])
+
+
+def test_attention_matches_high_precision_brute_force():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    Q, K, V = _attn_inputs(1, 3, 7, 5, 4, 540)
+    scale = 0.61
+    O, lse = oracle.attention_forward(Q, K, V, scale=scale, with_lse=True)
+    q, k, v = val(Q[0]), val(K[0]), val(V[0])
+    for i in range(3):
+        s = [mpmath.mpf(scale) * mpmath.fsum(mpmath.mpf(q[i, t]) * mpmath.mpf(k[j, t]) for t in range(5))
+             for j in range(7)]
+        e = [mpmath.exp(x) for x in s]
+        tot = mpmath.fsum(e)
+        assert abs(float(mpmath.log(tot)) - lse[0, i]) <= 1e-13
+        for c in range(4):
+            ref = mpmath.fsum(e[j] * mpmath.mpf(v[j, c]) for j in range(7)) / tot
+            assert abs(float(ref) - O[0, i, c]) <= 1e-13 * (1.0 + abs(float(ref)))
