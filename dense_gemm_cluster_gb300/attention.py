@@ -1,0 +1,64 @@
+"""Throughput of the fused attention forward (include/attention.h).
+
+    python -m dense_gemm_cluster_gb300.attention [--batch B] [--sq S] [--sk S] [--steps K]
+
+One JSON line per cluster size: TFLOP/s (4 * batch * sq * sk * d per launch:
+the two products) against the tensor roofline. Inputs: seeded N(0,1) bf16.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+
+
+def measure(batch=128, sq=4096, sk=4096, d=128, cluster=2, steps=10, warmup=3, device=0):
+    import numpy as np
+    import torch
+    from . import gemm, inputs
+    dev = torch.device("cuda", device)
+
+    def mk(seed, rows):
+        return torch.from_numpy(inputs.bf16_matrix(rows, d, "normal", seed).view(np.int16)).to(dev)
+
+    Q, K, V = mk(0, batch * sq), mk(1, batch * sk), mk(2, batch * sk)
+    O = torch.empty(batch * sq * d, dtype=torch.int16, device=dev)
+    lse = torch.empty(batch * sq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        assert gemm.attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, 0.0, 0, cluster, stream) == 0
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        st[i].record(stream)
+        gemm.attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, 0.0, 0, cluster, stream)
+        en[i].record(stream)
+    assert gemm.attention_forward_query_status(stream) == 0
+    ms = sum(a.elapsed_time(b) for a, b in zip(st, en)) / steps
+    flops = 4.0 * batch * sq * sk * d
+    peak = 1893.8
+    try:
+        with open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, ValueError, KeyError):
+        pass
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"kernel": "attention_fwd", "batch": batch, "sq": sq, "sk": sk, "d": d, "cluster": cluster, "ms": ms,
+            "TFLOPs": tf, "tensor_peak": peak, "frac": tf / peak}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--batch", type=int, default=128)
+    ap.add_argument("--sq", type=int, default=4096)
+    ap.add_argument("--sk", type=int, default=4096)
+    ap.add_argument("--steps", type=int, default=10)
+    args = ap.parse_args(argv)
+    for c in (1, 2, 4):
+        print(json.dumps(measure(args.batch, args.sq, args.sk, 128, c, args.steps)), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

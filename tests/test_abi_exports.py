@@ -1,4 +1,4 @@
-"""The C-ABI library builds, loads, and exports every entry point include/densegemm.h declares.
+"""The C-ABI library builds, loads, and exports every entry point the headers under include/ declare.
 
 Also checks the host-only planner (no GPU needed): validation and launch plans.
 """
@@ -25,7 +25,7 @@ def declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"\b((?:gemm|tma_bench)_\w+)\s*\(", text))
+            names |= set(re.findall(r"\b((?:gemm|tma_bench|stencil_1d|attention_forward)_\w+)\s*\(", text))
     return sorted(names)
 
 

@@ -1,0 +1,83 @@
+"""GPU parity of the fused attention forward against the fp64 oracle.
+
+O is a convex combination of V rows; P is rounded to bf16 before P V, so the
+bound is 1e-2 * max|V| (about four bf16 roundings); the log-sum-exp is
+accumulated in fp32 from unrounded probabilities and held to 1e-4 relative.
+K/V multicast only moves data: clusters of 2 and 4 must equal cluster 1 bit
+for bit.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(b, sq, sk, seed, k_growth=0.0):
+    from dense_gemm_cluster_gb300 import inputs
+    Q = inputs.bf16_matrix(b * sq, 128, "normal", seed).reshape(b, sq, 128)
+    Kf = inputs.bf16_bits_to_f32(inputs.bf16_matrix(b * sk, 128, "normal", seed + 1)).reshape(b, sk, 128).astype(np.float64)
+    if k_growth:
+        # keys grow along the sequence so each key tile raises the row max
+        Kf = Kf * (1.0 + k_growth * np.arange(sk)[None, :, None] / sk)
+    K = inputs.f64_to_bf16_bits(Kf).reshape(b, sk, 128)
+    V = inputs.bf16_matrix(b * sk, 128, "normal", seed + 2).reshape(b, sk, 128)
+    return Q, K, V
+
+
+def _run(Q, K, V, cluster, out_f32=0, scale=0.0):
+    import torch
+    from dense_gemm_cluster_gb300 import gemm
+    b, sq, _ = Q.shape
+    sk = K.shape[1]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    O = torch.full((b * sq * 128,), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    lse = torch.full((b * sq,), float("nan"), dtype=torch.float32, device="cuda")
+    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, 128, scale, out_f32, cluster)
+    assert s == gemm.GEMM_OK
+    assert gemm.attention_forward_query_status() == gemm.GEMM_OK
+    o = O.float().cpu().numpy().reshape(b, sq, 128).astype(np.float64)
+    return o, lse.cpu().numpy().reshape(b, sq).astype(np.float64)
+
+
+@pytest.mark.parametrize("b,sq,sk", [(2, 128, 128), (3, 300, 500), (1, 1000, 130), (2, 256, 2048), (1, 77, 1)])
+@pytest.mark.parametrize("cluster", [1, 2, 4])
+def test_attention_matches_oracle(b, sq, sk, cluster):
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    Q, K, V = _inputs(b, sq, sk, 100 + sq)
+    o, lse = _run(Q, K, V, cluster)
+    ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True)
+    vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+    assert np.isfinite(o).all()
+    assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
+    assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+
+
+def test_attention_rescales_when_the_row_max_grows():
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    Q, K, V = _inputs(2, 256, 1024, 7, k_growth=3.0)
+    for scale in (0.0, 0.35):
+        o, lse = _run(Q, K, V, 2, out_f32=1, scale=scale)
+        ref, ref_lse = oracle.attention_forward(Q, K, V, scale=scale if scale else None, with_lse=True)
+        vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+        assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
+        assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+
+
+def test_attention_multicast_is_bit_identical():
+    Q, K, V = _inputs(2, 512, 640, 9)
+    base, base_lse = _run(Q, K, V, 1, out_f32=1)
+    for c in (2, 4):
+        o, lse = _run(Q, K, V, c, out_f32=1)
+        assert np.array_equal(o, base) and np.array_equal(lse, base_lse)
+
+
+def test_attention_argument_errors():
+    import torch
+    from dense_gemm_cluster_gb300 import gemm
+    x = torch.zeros(128 * 128, dtype=torch.int16, device="cuda")
+    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 64) == gemm.GEMM_ERR_UNSUPPORTED
+    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 3) == gemm.GEMM_ERR_UNSUPPORTED
+    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 0, 128) == gemm.GEMM_ERR_INVALID_ARG
+    assert gemm.attention_forward_run(x.data_ptr() + 2, x, x, x, None, 1, 128, 128, 128) == gemm.GEMM_ERR_ALIGNMENT
