@@ -1,6 +1,7 @@
 """Throughput of the fused attention forward (include/attention.h).
 
-    python -m dense_gemm_cluster_gb300.attention [--batch B] [--sq S] [--sk S] [--steps K]
+    python -m dense_gemm_cluster_gb300.attention [--batch B] [--sq S] [--sk S] [--cluster C]
+                                                 [--steps K] [--warmup W]
 
 One JSON line per cluster size: TFLOP/s (4 * batch * sq * sk * d per launch:
 the two products) against the tensor roofline. Inputs: seeded N(0,1) bf16.
@@ -53,10 +54,12 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=128)
     ap.add_argument("--sq", type=int, default=4096)
     ap.add_argument("--sk", type=int, default=4096)
+    ap.add_argument("--cluster", type=int, choices=(1, 2, 4), default=None, help="one cluster size (default: all)")
     ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args(argv)
-    for c in (1, 2, 4):
-        print(json.dumps(measure(args.batch, args.sq, args.sk, 128, c, args.steps)), flush=True)
+    for c in ((args.cluster,) if args.cluster else (1, 2, 4)):
+        print(json.dumps(measure(args.batch, args.sq, args.sk, 128, c, args.steps, args.warmup)), flush=True)
     return 0
 
 

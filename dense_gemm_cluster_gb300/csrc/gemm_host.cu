@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kMaxSmemPerCta = 232448;        // 227 KB opt-in shared memory per block on sm_103
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int64_t kMinSplitBlocks = 16;         // k-blocks per cluster before a sub-wave problem is split wider
 
 thread_local std::string g_thread_error;
 
@@ -152,7 +153,21 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     p.tiles = tm * tn * batch;
     int64_t clusters = sm_count / (cm * cn);
     if (o.max_clusters > 0 && o.max_clusters < clusters) clusters = o.max_clusters;
-    if (p.tiles < clusters) clusters = p.tiles;
+    if (p.tiles < clusters) {
+        // Fewer tiles than clusters. Whole tiles leave the rest idle; when at most
+        // half the clusters would have one, a schedule that splits k-blocks (auto,
+        // stream-K) spreads them over more clusters, at least kMinSplitBlocks each
+        // so small problems stay compact. (Handing a partial to the finisher costs
+        // a few microseconds at the end of the kernel: 128 tiles on 152 SMs run
+        // faster whole.)
+        const int64_t num_kb = ceil_div(K, (int64_t)BK);
+        int64_t want = p.tiles;
+        if ((o.schedule == 0 || o.schedule == 2) && num_kb >= 2 && 2 * p.tiles <= clusters) {
+            const int64_t spread = p.tiles * num_kb / kMinSplitBlocks;
+            if (spread > want) want = spread;
+        }
+        if (want < clusters) clusters = want;
+    }
     p.clusters = clusters;
     const int64_t k_pad = ceil_div(K, BK) * BK;
     p.l2_to_sm_operand_bytes = p.tiles * cm * cn * k_pad * 2 * (dgc::BLOCK_M / gA + (BN / G) / gB);
@@ -569,12 +584,13 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
         clusters = pl.tiles;
         kp.clc = 1;
     }
-    cfg.gridDim = dim3((unsigned)(clusters * cs), 1, 1);
     // Stream-K tail (needs the co-residency the occupancy cap guarantees, and a workspace).
     if (o.schedule == 2 && h->no_alloc)
         return fail(&h->err, GEMM_ERR_UNSUPPORTED, "the stream-K tail needs a workspace; gemm_run_noalloc runs whole tiles");
     kp.dp_tiles = whole_tiles_for(o.schedule, pl.tiles, clusters, kp.num_kb, !h->no_alloc);
     kp.sk_iters = (pl.tiles - kp.dp_tiles) * kp.num_kb;
+    if (kp.sk_iters == 0 && o.schedule != 3 && clusters > pl.tiles) clusters = pl.tiles;   // whole tiles only
+    cfg.gridDim = dim3((unsigned)(clusters * cs), 1, 1);
     if (kp.sk_iters > 0) {
         const size_t slots = (size_t)(clusters * cs);
         const size_t ws_bytes = slots * dgc::BLOCK_M * BN * sizeof(float);

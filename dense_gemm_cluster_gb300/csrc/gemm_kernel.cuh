@@ -474,14 +474,15 @@ __device__ __forceinline__ void store_tile(const KernelParams& p, const CUtensor
             for (int i = 0; i < 32; ++i) v[(CW - 32) + i] = __uint_as_float(r[i]);
         }
         if (FIXUP) {
-            // Add the other contributors' partials, in cluster order.
+            // Add the other contributors' partials, in cluster order ([column / 4][row][4] slots).
             for (int i = 0; i < e.contrib_count; ++i) {
-                const float4* src = reinterpret_cast<const float4*>(
-                    p.workspace + (((long long)(e.contrib_first + i) * e.cs + e.rank) * BLOCK_M + e.trow) *
-                                      (long long)BN + c * CW);
+                const float4* src =
+                    reinterpret_cast<const float4*>(
+                        p.workspace + ((long long)(e.contrib_first + i) * e.cs + e.rank) * (long long)(BLOCK_M * BN)) +
+                    (long long)(c * (CW / 4)) * BLOCK_M + e.trow;
 #pragma unroll
                 for (int j = 0; j < CW / 4; ++j) {
-                    const float4 a = src[j];
+                    const float4 a = src[j * BLOCK_M];
                     v[4 * j] += a.x;
                     v[4 * j + 1] += a.y;
                     v[4 * j + 2] += a.z;
@@ -787,8 +788,10 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int row = m0 + trow;                    // global row this thread stores
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             if (w.kind == WORK_PARTIAL) {
-                // Part of a tile another cluster finishes: park the fp32 partial.
-                float* dst = p.workspace + (slot * BLOCK_M + trow) * (long long)BN;
+                // Part of a tile another cluster finishes: park the fp32 partial. A slot
+                // holds [column / 4][row][4] floats, so the 32 rows of a warp write 512
+                // contiguous bytes per store.
+                float4* dst = reinterpret_cast<float4*>(p.workspace + slot * (long long)(BLOCK_M * BN)) + trow;
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32cols(t_row + c * 32, r);
@@ -801,11 +804,11 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             else        mbar_arrive_local(tempty_addr + 8u * acc);
                         }
                     }
-                    float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                            __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        dst[(c * 8 + j) * BLOCK_M] =
+                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                 }
                 __threadfence();
                 epilogue_bar();

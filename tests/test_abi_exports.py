@@ -146,3 +146,18 @@ def test_plan_stream_k_tail(lib):
     assert plan(lib, 64, 64, 64, schedule=4)[0] == 1
     s, p = plan(lib, 4096, 4096, 4096, sm=152, schedule="clc")
     assert s == 0 and p.stream_k_tiles == 0
+
+
+def test_plan_sub_wave_spread(lib):
+    # 6 tiles of 128x128 with 64 k-blocks each on 152 SMs: split 16 k-blocks a cluster
+    s, p = plan(lib, 768, 128, 8192, sm=152, block_n=128)
+    assert s == 0 and p.tiles == 6 and p.clusters == 24 and p.stream_k_tiles == 6
+    s, p = plan(lib, 256, 256, 2048, sm=152)       # 2 tiles x 32 k-blocks: 4 clusters of 16
+    assert p.tiles == 2 and p.clusters == 4 and p.stream_k_tiles == 2
+    # whole tiles: more than half the clusters busy, a whole-tile schedule, or < 16 k-blocks a cluster
+    s, p = plan(lib, 16384, 128, 8192, sm=152, block_n=128)
+    assert p.tiles == 128 and p.clusters == 128 and p.stream_k_tiles == 0
+    s, p = plan(lib, 768, 128, 8192, sm=152, block_n=128, schedule="dp")
+    assert p.clusters == 6 and p.stream_k_tiles == 0
+    s, p = plan(lib, 256, 256, 256, sm=152, mode="mcast", mcast_b=1, cluster_m=2)
+    assert p.tiles == 1 and p.clusters == 1

@@ -158,3 +158,22 @@ def test_stream_k_with_multicast_clusters_is_deterministic(G):
     b = _run(G, p, schedule="stream_k", mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2, max_clusters=9)
     assert_close(a, p.reference(), 704, "f32", "stream-K 2x2 multicast")
     assert np.array_equal(a, b)          # partials are summed in a fixed order
+
+
+@pytest.mark.parametrize("M,N,K,opts", [
+    (300, 200, 8192, dict(block_n=128)),                                       # 6 tiles over 24 clusters
+    (1024, 128, 4096, dict(block_n=128, mode="mcast", mcast_b=1, cluster_m=4)),  # 2 cluster tiles over 4
+    (130, 1000, 3000, dict(block_n=256)),                                      # ragged K and tiles
+])
+def test_sub_wave_problem_spreads_over_more_clusters(G, M, N, K, opts):
+    # Fewer tiles than clusters: the auto schedule splits k-blocks over more clusters
+    # (at least 16 each); partials are summed in a fixed order, so reruns are bitwise equal.
+    import torch
+    s, plan = G.gemm_plan(G.make_options(layout_a="row", layout_b="row", out_type="f32", **opts), M, N, K, 1,
+                          torch.cuda.get_device_properties(0).multi_processor_count)
+    assert s == 0 and plan.clusters > plan.tiles and plan.stream_k_tiles == plan.tiles
+    p = Problem(M, N, K, la="row", lb="row", out="f32", seed=11)
+    a = _run(G, p, **opts)
+    b = _run(G, p, **opts)
+    assert_close(a, p.reference(), K, "f32", f"sub-wave {M}x{N}x{K} {opts}")
+    assert np.array_equal(a, b)

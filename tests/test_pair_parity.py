@@ -94,3 +94,12 @@ def test_pair_stream_k_tail(G, cm, cn, ma, mb):
     got = _run(G, p, 1.0, 0.5, cta_group=2, cluster_m=cm, cluster_n=cn, mode="mcast", mcast_a=ma, mcast_b=mb,
                schedule="stream_k", max_clusters=5)
     assert_close(got, p.reference(1.0, 0.5), 1152, "bf16", f"pair stream-K {cm}x{cn}")
+
+
+def test_pair_sub_wave_problem_spreads_over_more_clusters(G):
+    # 2 pair tiles of 256x256 with 64 k-blocks each: the auto schedule splits them over more pairs
+    p = Problem(512, 256, 8192, la="row", lb="col", out="bf16", beta=0.5, seed=19)
+    a = _run(G, p, 1.0, 0.5, cta_group=2, cluster_m=2)
+    b = _run(G, p, 1.0, 0.5, cta_group=2, cluster_m=2)
+    assert_close(a, p.reference(1.0, 0.5), 8192, "bf16", "pair sub-wave")
+    assert np.array_equal(a, b)
