@@ -6,15 +6,24 @@
 // of them, every issuer arming each receiver's mbarrier (through mapa) before
 // it issues (section 深度机制剖析).
 //
-// One CTA = one 128-row query tile. Roles (224 threads):
-//   warp 0      producer: the Q tile once, then K tiles into a 2-stage ring
-//   warp 6      producer: V tiles into the same ring
-//   warp 1      TMEM allocation and MMA issue: S_j = Q K_j^T into one of two
-//               TMEM score buffers, O += P_j V_j into the TMEM output
-//   warps 2..5  softmax: one query row per thread; online softmax in base 2
-//               with a running reference max that is moved (and O rescaled in
-//               TMEM) only when a row's max grows by more than 2^8; P_j goes
-//               to shared memory as bf16; finally O / l and the log-sum-exp.
+// One CTA = two 128-row query tiles (Q0, Q1) of one (batch, head). Tensor
+// memory holds both score tiles and both output accumulators (4 x 128 of its
+// 512 columns); the probabilities P_i overwrite the first 64 columns of S_i
+// as packed bf16 and feed O_i += P_i V_j straight from tensor memory, so no
+// score or probability ever touches shared memory.
+//
+// Roles (384 threads):
+//   warp 0      producer: Q0 and Q1 once, then K_0, V_0, K_1, V_1, ... into a
+//               ring of four 32 KB slots (this CTA's slice of each, multicast)
+//   warp 1      TMEM allocation and MMA issue, per key tile j in the order
+//               O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T
+//               so the tensor core works on one tile while the other tile's
+//               softmax runs (the two softmaxes take turns on the exp unit)
+//   warps 2, 3  idle
+//   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1: one query row
+//               per thread, online softmax in base 2 with a reference max that
+//               moves (rescaling O in TMEM) only when the row max grows by
+//               more than 2^8; at the end O / l and the log-sum-exp.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -31,14 +40,16 @@ namespace {
 
 using namespace dgc;
 
-constexpr int TQ = 128;                  // queries per CTA
+constexpr int TQ = 128;                  // queries per tile
+constexpr int QT = 2;                    // query tiles per CTA
 constexpr int TK = 128;                  // keys per tile
 constexpr int HD = 128;                  // head dimension
-constexpr int THREADS = 224;
-constexpr uint32_t TILE_BYTES = TQ * HD * 2;    // 32 KB: Q, K, V and P tiles alike
-constexpr uint32_t ATOM_BYTES = TQ * 128;       // one 64-element swizzle atom of a 128-row tile
-constexpr int KV_STAGES = 2;
+constexpr int THREADS = 384;
+constexpr uint32_t TILE_BYTES = 128 * HD * 2;   // 32 KB: a Q, K or V tile
+constexpr uint32_t ATOM_BYTES = 128 * 128;      // one 64-element swizzle atom of a 128-row tile
+constexpr int NS = 4;                           // ring slots; K and V tiles alternate
 constexpr float RESCALE_THRESHOLD = 8.0f;       // log2 units: move the reference max past 2^8 growth
+constexpr size_t SMEM_BYTES = 1024 + (QT + NS) * TILE_BYTES + 16 * 8 + 16;
 
 __device__ unsigned int g_attn_status[4];
 
@@ -80,41 +91,35 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sK = sQ + TILE_BYTES;                       // KV_STAGES tiles
-    uint8_t* sV = sK + KV_STAGES * TILE_BYTES;           // KV_STAGES tiles
-    uint8_t* sP = sV + KV_STAGES * TILE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + TILE_BYTES);
+    uint8_t* sQ = smem;                                   // QT tiles
+    uint8_t* ring = sQ + QT * TILE_BYTES;                 // NS slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + NS * TILE_BYTES);
     uint64_t* q_full = bars;                 // 1
-    uint64_t* k_full = bars + 1;             // KV_STAGES
-    uint64_t* v_full = bars + 3;             // KV_STAGES
-    uint64_t* kv_empty = bars + 5;           // KV_STAGES
-    uint64_t* s_full = bars + 7;             // 2
-    uint64_t* s_empty = bars + 9;            // 2
-    uint64_t* p_full = bars + 11;            // 1
-    uint64_t* pv_done = bars + 12;           // 1
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+    uint64_t* kv_full = bars + 1;            // NS
+    uint64_t* kv_empty = bars + 1 + NS;      // NS
+    uint64_t* s_full = bars + 1 + 2 * NS;    // QT: S_i written
+    uint64_t* p_full = s_full + QT;          // QT: P_i written (and O_i rescaled)
+    uint64_t* pv_done = p_full + QT;         // QT: O_i += P_i V_j completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_done + QT);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = p.cluster;
     const uint32_t rank = c > 1 ? cluster_ctarank() : 0u;
     const uint16_t all = (uint16_t)((1u << c) - 1u);
     const int b = blockIdx.y;
-    const int q0 = blockIdx.x * TQ;
+    const int q0 = blockIdx.x * (QT * TQ);
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(q_full), 1);
-        for (int s = 0; s < KV_STAGES; ++s) {
-            mbar_init(smem_u32(&k_full[s]), (uint32_t)c);    // one arm per issuer of a slice
-            mbar_init(smem_u32(&v_full[s]), (uint32_t)c);
-            mbar_init(smem_u32(&kv_empty[s]), (uint32_t)c);  // one release per consumer CTA
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&kv_full[s]), (uint32_t)c);    // one arm per issuer of a slice
+            mbar_init(smem_u32(&kv_empty[s]), (uint32_t)c);   // one release per consumer CTA
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < QT; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&s_empty[i]), 4);
+            mbar_init(smem_u32(&p_full[i]), 4);
+            mbar_init(smem_u32(&pv_done[i]), 1);
         }
-        mbar_init(smem_u32(p_full), 4);
-        mbar_init(smem_u32(pv_done), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -125,194 +130,179 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     __syncthreads();
     if (c > 1) cluster_sync();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;        // columns: S0 [0,128), S1 [128,256), O [256,384)
+    const uint32_t tmem = *tmem_slot;        // columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
 
-    if ((warp == 0 || warp == 6) && lane == 0) {
-        // ---------------------------------------------------------------- producers
-        const bool is_k = warp == 0;
-        const CUtensorMap* tm = is_k ? &tmK : &tmV;
-        prefetch_tmap(tm);
-        if (is_k) {
-            prefetch_tmap(&tmQ);
-            mbar_arrive_expect_tx_local(smem_u32(q_full), TILE_BYTES);
-            tma_load_4d(smem_u32(sQ), &tmQ, smem_u32(q_full), 0, q0, 0, b);
-        }
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------------- producer
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        mbar_arrive_expect_tx_local(smem_u32(q_full), QT * TILE_BYTES);
+        for (int i = 0; i < QT; ++i)
+            tma_load_4d(smem_u32(sQ + i * TILE_BYTES), &tmQ, smem_u32(q_full), 0, q0 + i * TQ, 0, b);
         // This CTA's slice of each shared tile. K (K-major, 2 atoms): whole atoms
         // first, then rows within an atom. V (MN-major, 2 boxes of 64 d columns x 128
         // keys): a band of key rows of both boxes.
-        int atom0 = 0, r0 = 0, rows = TK;
-        if (is_k) {
-            if (c <= 2) { atom0 = (int)rank; }
-            else { atom0 = (int)rank / (c / 2); r0 = ((int)rank % (c / 2)) * (TK / (c / 2)); }
-        } else {
-            rows = TK / c;
-            r0 = (int)rank * rows;
-        }
+        int k_atom0 = 0, k_r0 = 0;
+        if (c <= 2) { k_atom0 = (int)rank; }
+        else { k_atom0 = (int)rank / (c / 2); k_r0 = ((int)rank % (c / 2)) * (TK / (c / 2)); }
+        const int v_r0 = (int)rank * (TK / c);
         const uint32_t slice_bytes = TILE_BYTES / (uint32_t)c;
-        uint64_t* full = is_k ? k_full : v_full;
-        uint8_t* base = is_k ? sK : sV;
-        for (int j = 0; j < p.n_kv; ++j) {
-            const int s = j % KV_STAGES;
-            const uint32_t ph = (uint32_t)(j / KV_STAGES) & 1u;
+        const int loads = 2 * p.n_kv;
+        for (int n = 0; n < loads; ++n) {
+            const int s = n % NS;
+            const uint32_t ph = (uint32_t)(n / NS) & 1u;
             if (!attn_wait(smem_u32(&kv_empty[s]), ph ^ 1u, p, 1)) break;
-            const uint32_t fb = smem_u32(&full[s]);
+            const uint32_t fb = smem_u32(&kv_full[s]);
             for (int r = 0; r < c; ++r) {
                 if (r == (int)rank) mbar_arrive_expect_tx_local(fb, slice_bytes);
                 else mbar_arrive_expect_tx_cluster(mapa(fb, (uint32_t)r), slice_bytes);
             }
-            const uint32_t tile = smem_u32(base + s * TILE_BYTES);
-            const int key0 = j * TK;
-            if (is_k) {
-                const uint32_t dst = tile + (uint32_t)(atom0 * ATOM_BYTES + r0 * 128);
-                if (c > 1) tma_load_4d_mcast(dst, tm, fb, 0, key0 + r0, atom0, b, all);
-                else       tma_load_4d(dst, tm, fb, 0, key0 + r0, 0, b);
+            const uint32_t tile = smem_u32(ring + s * TILE_BYTES);
+            const int key0 = (n >> 1) * TK;
+            if ((n & 1) == 0) {
+                const uint32_t dst = tile + (uint32_t)(k_atom0 * ATOM_BYTES + k_r0 * 128);
+                if (c > 1) tma_load_4d_mcast(dst, &tmK, fb, 0, key0 + k_r0, k_atom0, b, all);
+                else       tma_load_4d(dst, &tmK, fb, 0, key0, 0, b);
             } else {
                 for (int box = 0; box < HD / 64; ++box) {
-                    const uint32_t dst = tile + (uint32_t)(box * TK * 128 + r0 * 128);
-                    if (c > 1) tma_load_3d_mcast(dst, tm, fb, box * 64, key0 + r0, b, all);
-                    else       tma_load_3d(dst, tm, fb, box * 64, key0 + r0, b);
+                    const uint32_t dst = tile + (uint32_t)(box * TK * 128 + v_r0 * 128);
+                    if (c > 1) tma_load_3d_mcast(dst, &tmV, fb, box * 64, key0 + v_r0, b, all);
+                    else       tma_load_3d(dst, &tmV, fb, box * 64, key0, b);
                 }
             }
         }
-        // Every stage this thread filled is released by all receivers before exit.
-        for (int j = p.n_kv; j < p.n_kv + KV_STAGES; ++j) {
-            const int s = j % KV_STAGES;
-            if (!attn_wait(smem_u32(&kv_empty[s]), ((uint32_t)(j / KV_STAGES) & 1u) ^ 1u, p, 1)) break;
+        // Every slot this thread filled is released by all receivers before exit.
+        for (int n = loads; n < loads + NS; ++n) {
+            const int s = n % NS;
+            if (!attn_wait(smem_u32(&kv_empty[s]), ((uint32_t)(n / NS) & 1u) ^ 1u, p, 1)) break;
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------------- MMA issuer
         const uint32_t idesc_s = instr_desc_bf16(TQ, TK, false, false);    // Q (K-major) x K^T (K-major)
-        const uint32_t idesc_o = instr_desc_bf16(TQ, HD, false, true);     // P (K-major) x V (MN-major)
-        const uint64_t dq = smem_desc_sw128(smem_u32(sQ), false, 0);
-        const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), false, 0);
-        const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), true, TK * 128);
-        const uint64_t dp = smem_desc_sw128(smem_u32(sP), false, 0);
-        const uint16_t release_mask = all;
+        const uint32_t idesc_o = instr_desc_bf16(TQ, HD, false, true);     // P (TMEM) x V (MN-major)
+        const uint64_t ring_k = smem_desc_sw128(smem_u32(ring), false, 0);
+        const uint64_t ring_v = smem_desc_sw128(smem_u32(ring), true, TK * 128);
         bool ok = attn_wait(smem_u32(q_full), 0, p, 2);
-        auto issue_s = [&](int j) -> bool {
-            const int s = j % KV_STAGES;
-            if (!attn_wait(smem_u32(&k_full[s]), (uint32_t)(j / KV_STAGES) & 1u, p, 3)) return false;
-            const int sb = j & 1;
-            if (!attn_wait(smem_u32(&s_empty[sb]), ((uint32_t)(j >> 1) & 1u) ^ 1u, p, 4)) return false;
-            tc_fence_after();
-            const uint64_t dk = dk0 + ((s * TILE_BYTES) >> 4);
+        // S_i = Q_i K_j^T; the second tile's commit releases K_j's slot.
+        auto issue_s = [&](int i, int j) -> bool {
+            const int n = 2 * j, s = n % NS;
+            if (i == 0) {
+                if (!attn_wait(smem_u32(&kv_full[s]), (uint32_t)(n / NS) & 1u, p, 3)) return false;
+                tc_fence_after();
+            }
+            const uint64_t dq = smem_desc_sw128(smem_u32(sQ + i * TILE_BYTES), false, 0);
+            const uint64_t dk = ring_k + ((s * TILE_BYTES) >> 4);
 #pragma unroll
             for (int k = 0; k < HD / 16; ++k)
-                mma_bf16<1>(tmem + sb * TK, dq + kmajor_koff(k), dk + kmajor_koff(k), idesc_s, k > 0 ? 1u : 0u);
-            mma_commit<1>(smem_u32(&s_full[sb]));
+                mma_bf16<1>(tmem + i * TK, dq + kmajor_koff(k), dk + kmajor_koff(k), idesc_s, k > 0 ? 1u : 0u);
+            mma_commit<1>(smem_u32(&s_full[i]));
+            if (i == QT - 1) {
+                if (c > 1) mma_commit_mcast<1>(smem_u32(&kv_empty[s]), all);
+                else       mma_commit<1>(smem_u32(&kv_empty[s]));
+            }
             return true;
         };
-        if (ok) ok = issue_s(0);
-        for (int j = 0; ok && j < p.n_kv; ++j) {
-            if (j + 1 < p.n_kv && !issue_s(j + 1)) { ok = false; break; }
-            const int s = j % KV_STAGES;
-            if (!attn_wait(smem_u32(p_full), (uint32_t)j & 1u, p, 5)) { ok = false; break; }
-            if (!attn_wait(smem_u32(&v_full[s]), (uint32_t)(j / KV_STAGES) & 1u, p, 6)) { ok = false; break; }
+        // O_i += P_i V_j with P_i from TMEM; the second tile's commit releases V_j's slot.
+        auto issue_pv = [&](int i, int j) -> bool {
+            const int n = 2 * j + 1, s = n % NS;
+            if (i == 0 && !attn_wait(smem_u32(&kv_full[s]), (uint32_t)(n / NS) & 1u, p, 4)) return false;
+            if (!attn_wait(smem_u32(&p_full[i]), (uint32_t)j & 1u, p, 5)) return false;
             tc_fence_after();
-            const uint64_t dv = dv0 + ((s * TILE_BYTES) >> 4);
+            const uint64_t dv = ring_v + ((s * TILE_BYTES) >> 4);
 #pragma unroll
             for (int k = 0; k < TK / 16; ++k)
-                mma_bf16<1>(tmem + 2 * TK, dp + kmajor_koff(k), dv + mnmajor_koff(k), idesc_o,
+                mma_bf16_ts(tmem + 2 * TK + i * HD, tmem + i * TK + k * 8, dv + mnmajor_koff(k), idesc_o,
                             (j > 0 || k > 0) ? 1u : 0u);
-            mma_commit<1>(smem_u32(pv_done));
-            // K_j and V_j are consumed: release the stage to every CTA that fills it.
-            if (c > 1) mma_commit_mcast<1>(smem_u32(&kv_empty[s]), release_mask);
-            else       mma_commit<1>(smem_u32(&kv_empty[s]));
+            mma_commit<1>(smem_u32(&pv_done[i]));
+            if (i == QT - 1) {
+                if (c > 1) mma_commit_mcast<1>(smem_u32(&kv_empty[s]), all);
+                else       mma_commit<1>(smem_u32(&kv_empty[s]));
+            }
+            return true;
+        };
+        if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
+        for (int j = 0; ok && j < p.n_kv; ++j) {
+            const bool more = j + 1 < p.n_kv;
+            ok = issue_pv(0, j) && (!more || issue_s(0, j + 1)) && issue_pv(1, j) && (!more || issue_s(1, j + 1));
         }
-        (void)ok;
-    } else if (warp >= 2 && warp <= 5) {
+    } else if (warp >= 4) {
         // ---------------------------------------------------------------- softmax
+        const int ti = (warp - 4) >> 2;              // query tile
         const int qd = warp & 3;                     // TMEM lane quadrant
         const int row = qd * 32 + lane;              // query row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+        const uint32_t tS = lane_base + ti * TK;
+        const uint32_t tO = lane_base + 2 * TK + ti * HD;
+        const float cs = p.scale_log2;
         float m_ref = -INFINITY;                     // reference max, base-2 units
-        float l = 0.0f;                              // running sum of exp2(x - m_ref)
+        float l = 0.0f;                              // running sum of 2^(x - m_ref)
         bool ok = true;
         for (int j = 0; j < p.n_kv; ++j) {
-            const int sb = j & 1;
-            if (!attn_wait(smem_u32(&s_full[sb]), (uint32_t)(j >> 1) & 1u, p, 7)) { ok = false; break; }
+            if (!attn_wait(smem_u32(&s_full[ti]), (uint32_t)j & 1u, p, 7)) { ok = false; break; }
             tc_fence_after();
-            float x[TK];
-#pragma unroll
-            for (int cchunk = 0; cchunk < TK / 32; ++cchunk) {
-                uint32_t r[32];
-                tmem_ld_32cols(lane_base + sb * TK + cchunk * 32, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[cchunk * 32 + i] = __uint_as_float(r[i]) * p.scale_log2;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_local(smem_u32(&s_empty[sb]));
+            uint32_t x[TK];
+            tmem_ld_128cols_wait(tS, x);
             const int valid = p.sk - j * TK;         // keys of this tile inside the sequence
-            float mx = -INFINITY;
+            if (valid < TK) {
 #pragma unroll
-            for (int i = 0; i < TK; ++i) {
-                if (i >= valid) x[i] = -INFINITY;
-                mx = fmaxf(mx, x[i]);
+                for (int i = 0; i < TK; ++i)
+                    if (i >= valid) x[i] = __float_as_uint(-INFINITY);
             }
+            float mx = __uint_as_float(x[0]);
+#pragma unroll
+            for (int i = 1; i < TK; ++i) mx = fmaxf(mx, __uint_as_float(x[i]));
+            const float m_new = mx * cs;
             float alpha = 1.0f;                      // factor for O and l when the reference moves
             if (j == 0) {
-                m_ref = mx;
-            } else if (mx > m_ref + RESCALE_THRESHOLD) {
-                alpha = exp2f(m_ref - mx);
-                m_ref = mx;
+                m_ref = m_new;
+            } else if (m_new > m_ref + RESCALE_THRESHOLD) {
+                alpha = ex2_approx(m_ref - m_new);
+                m_ref = m_new;
             }
             l *= alpha;
-            uint32_t pk[TK / 2];
+            const float neg = -m_ref;
+            // P over the first 64 columns of S: keys 2c and 2c+1 packed in column c.
 #pragma unroll
-            for (int i = 0; i < TK / 2; ++i) {
-                const float p0 = exp2f(x[2 * i] - m_ref);
-                const float p1 = exp2f(x[2 * i + 1] - m_ref);
-                l += p0 + p1;
-                pk[i] = pack_bf16x2(p0, p1);
+            for (int h = 0; h < TK / 32; ++h) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(x[32 * h + 2 * i]), cs, neg));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(x[32 * h + 2 * i + 1]), cs, neg));
+                    l += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st_16cols(tS + h * 16, pk);
             }
-            if (j > 0) {
-                // P_{j-1} V_{j-1} has completed: O is stable and the P buffer is free.
-                if (!attn_wait(smem_u32(pv_done), (uint32_t)(j - 1) & 1u, p, 8)) { ok = false; break; }
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                // O_i is stable once P_i V_{j-1} has completed.
+                if (!attn_wait(smem_u32(&pv_done[ti]), (uint32_t)(j - 1) & 1u, p, 8)) { ok = false; break; }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-                    for (int cchunk = 0; cchunk < HD / 32; ++cchunk) {
-                        uint32_t r[32];
-                        const uint32_t ta = lane_base + 2 * TK + cchunk * 32;
-                        tmem_ld_32cols(ta, r);
-                        tmem_ld_wait();
+                for (int h = 0; h < HD / 32; ++h) {
+                    uint32_t r[32];
+                    tmem_ld_32cols_wait(tO + h * 32, r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st_32cols(ta, r);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    tmem_st_32cols(tO + h * 32, r);
                 }
             }
-            // P row into the K-major swizzled A-operand tile: keys 0-63 in atom 0, 64-127 in atom 1;
-            // 16-byte chunk g of row r sits at chunk g ^ (r % 8).
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-                uint8_t* rowp = sP + a * ATOM_BYTES + row * 128;
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const int w = a * 32 + g * 4;
-                    *reinterpret_cast<uint4*>(rowp + ((g ^ (row & 7)) << 4)) =
-                        make_uint4(pk[w], pk[w + 1], pk[w + 2], pk[w + 3]);
-                }
-            }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_local(smem_u32(p_full));
+            if (lane == 0) mbar_arrive_local(smem_u32(&p_full[ti]));
         }
         // Final normalisation: O / l, and lse = (m_ref + log2 l) * ln 2.
-        if (ok && attn_wait(smem_u32(pv_done), (uint32_t)(p.n_kv - 1) & 1u, p, 9)) {
+        if (ok && attn_wait(smem_u32(&pv_done[ti]), (uint32_t)(p.n_kv - 1) & 1u, p, 9)) {
             tc_fence_after();
-            const int q = q0 + row;
+            const int q = q0 + ti * TQ + row;
             const float inv = 1.0f / l;
-            for (int cchunk = 0; cchunk < HD / 32; ++cchunk) {
+            for (int h = 0; h < HD / 32; ++h) {
                 uint32_t r[32];
-                tmem_ld_32cols(lane_base + 2 * TK + cchunk * 32, r);
-                tmem_ld_wait();
+                tmem_ld_32cols_wait(tO + h * 32, r);
                 if (q < p.sq) {
-                    const long long off = ((long long)b * p.sq + q) * HD + cchunk * 32;
+                    const long long off = ((long long)b * p.sq + q) * HD + h * 32;
                     if (p.out_f32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
 #pragma unroll
@@ -415,12 +405,11 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     p.out = O;
     p.lse = lse;
     p.timeout_ns = 2000000000ull;
-    const size_t smem = 1024 + 6 * TILE_BYTES + 14 * 8 + 16;
     void* fn = reinterpret_cast<void*>(&attention_fwd_kernel);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));
-    long long qtiles = (sq + TQ - 1) / TQ;
-    qtiles = (qtiles + cluster - 1) / cluster * cluster;    // whole clusters; extra tiles store nothing
+    long long ctas = (sq + QT * TQ - 1) / (QT * TQ);
+    ctas = (ctas + cluster - 1) / cluster * cluster;      // whole clusters; extra CTAs store nothing
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cudaLaunchAttribute attr[1];
@@ -428,9 +417,9 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     attr[0].val.clusterDim.x = cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)qtiles, (unsigned)batch, 1);
+    cfg.gridDim = dim3((unsigned)ctas, (unsigned)batch, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -449,6 +438,6 @@ extern "C" gemm_status_t attention_forward_query_status(void* stream) {
     if (w[0] == 0) return GEMM_OK;
     unsigned int z[4] = {0, 0, 0, 0};
     cudaMemcpyToSymbol(g_attn_status, z, sizeof z);
-    snprintf(g_attn_err, sizeof g_attn_err, "attention: bounded wait %u expired (q tile %u, batch %u)", w[0], w[1], w[2]);
+    snprintf(g_attn_err, sizeof g_attn_err, "attention: bounded wait %u expired (q block %u, batch %u)", w[0], w[1], w[2]);
     return GEMM_ERR_DEVICE_TIMEOUT;
 }
