@@ -249,9 +249,16 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 for (int i = 0; i < TK; ++i)
                     if (i >= valid) x[i] = __float_as_uint(-INFINITY);
             }
-            float mx = __uint_as_float(x[0]);
+            // Row max: eight independent chains of three-input maxima.
+            float m8[8];
 #pragma unroll
-            for (int i = 1; i < TK; ++i) mx = fmaxf(mx, __uint_as_float(x[i]));
+            for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1]));
+#pragma unroll
+            for (int i = 16; i < TK; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    m8[k] = max3f(m8[k], __uint_as_float(x[i + 2 * k]), __uint_as_float(x[i + 2 * k + 1]));
+            const float mx = max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             const float m_new = mx * cs;
             float alpha = 1.0f;                      // factor for O and l when the reference moves
             if (j == 0) {
@@ -260,20 +267,33 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 alpha = ex2_approx(m_ref - m_new);
                 m_ref = m_new;
             }
-            l *= alpha;
-            const float neg = -m_ref;
             // P over the first 64 columns of S: keys 2c and 2c+1 packed in column c.
+            // Pairs of keys go through packed fp32 arithmetic: x * scale - m_ref in one
+            // fma.f32x2, the row sum in two f32x2 accumulators.
+            const uint64_t cs2 = f32x2(cs, cs);
+            const uint64_t neg2 = f32x2(-m_ref, -m_ref);
+            uint64_t ls2[2] = {f32x2(0.0f, 0.0f), f32x2(0.0f, 0.0f)};
 #pragma unroll
             for (int h = 0; h < TK / 32; ++h) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(x[32 * h + 2 * i]), cs, neg));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(x[32 * h + 2 * i + 1]), cs, neg));
-                    l += p0 + p1;
+                    const uint64_t t = fma_f32x2(
+                        f32x2(__uint_as_float(x[32 * h + 2 * i]), __uint_as_float(x[32 * h + 2 * i + 1])), cs2, neg2);
+                    float t0, t1;
+                    f32x2_split(t, t0, t1);
+                    const float p0 = ex2_approx(t0);
+                    const float p1 = ex2_approx(t1);
+                    ls2[i & 1] = add_f32x2(ls2[i & 1], f32x2(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st_16cols(tS + h * 16, pk);
+            }
+            {
+                float a0, a1, b0, b1;
+                f32x2_split(ls2[0], a0, a1);
+                f32x2_split(ls2[1], b0, b1);
+                l = fmaf(l, alpha, (a0 + a1) + (b0 + b1));
             }
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
                 // O_i is stable once P_i V_{j-1} has completed.

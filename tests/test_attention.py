@@ -81,3 +81,26 @@ def test_attention_argument_errors():
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 3) == gemm.GEMM_ERR_UNSUPPORTED
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 0, 128) == gemm.GEMM_ERR_INVALID_ARG
     assert gemm.attention_forward_run(x.data_ptr() + 2, x, x, x, None, 1, 128, 128, 128) == gemm.GEMM_ERR_ALIGNMENT
+
+
+def test_attention_row_max_sees_every_column():
+    # Query row r and key k share a large component when r = k (mod 128): every row has
+    # a score of ~200 (base 2) at column r mod 128 of each key tile and ~0 elsewhere.
+    # Over a tile's 128 rows the spike visits every column; a row max that missed a
+    # column would leave 2^(~200) in P, which overflows fp32.
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    b, sq, sk, d = 1, 256, 512, 128
+    amp = float(np.sqrt(200.0 / np.log2(np.e)))
+    noise = lambda rows, seed: inputs.bf16_bits_to_f32(inputs.bf16_matrix(rows, d, "normal", seed)).astype(np.float64) * 0.05
+    eye = lambda rows: np.eye(d)[np.arange(rows) % d] * amp
+    Q = inputs.f64_to_bf16_bits(eye(sq) + noise(sq, 31)).reshape(b, sq, d)
+    K = inputs.f64_to_bf16_bits(eye(sk) + noise(sk, 32)).reshape(b, sk, d)
+    V = inputs.bf16_matrix(sk, d, "normal", 33).reshape(b, sk, d)
+    for cluster in (1, 2):
+        o, lse = _run(Q, K, V, cluster, out_f32=1, scale=1.0)
+        ref, ref_lse = oracle.attention_forward(Q, K, V, scale=1.0, with_lse=True)
+        assert np.isfinite(o).all() and np.isfinite(lse).all()
+        vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+        assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
+        assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
