@@ -34,7 +34,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from dense_gemm_cluster_gb300 import inputs, traffic  # noqa: E402
-from dense_gemm_cluster_gb300.workloads import DEFAULT, WORKLOADS, Workload  # noqa: E402
+from dense_gemm_cluster_gb300.workloads import (ATTENTION_WORKLOADS, DEFAULT, WORKLOADS,  # noqa: E402
+                                                AttentionWorkload, Workload)
 
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense-BF16 peak; L2→SM bytes vs unicast"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
@@ -42,6 +43,7 @@ L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 129 << 20          # GB300 L2 (126 MiB usable); inputs above this need no flush
 KERNEL_SOURCES = ["dense_gemm_cluster_gb300/csrc/gemm_kernel.cuh", "dense_gemm_cluster_gb300/csrc/ptx.cuh",
                   "dense_gemm_cluster_gb300/csrc/gemm_host.cu"]
+ATTN_KERNEL_SOURCES = ["dense_gemm_cluster_gb300/csrc/attention.cu", "dense_gemm_cluster_gb300/csrc/ptx.cuh"]
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -87,15 +89,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, sources=KERNEL_SOURCES):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
@@ -104,7 +106,7 @@ def recorded_traffic(workload: str):
     except (OSError, ValueError):
         return None
     rec = recs.get(workload)
-    if not rec or rec.get("kernel_sha") != kernel_source_hash():
+    if not rec or rec.get("kernel_sha") != kernel_source_hash(sources):
         return None
     return rec
 
@@ -455,13 +457,203 @@ def e2e_through_host_api(g, p: DeviceProblem, args, device, stream, dist):
             "ms_per_step": 1e3 * elapsed / steps}
 
 
+# ---------------------------------------------------------------- fused attention workloads
+ATTN_METRIC = "attention forward TFLOP/s at 1 GB300 and % of dense-BF16 peak"
+
+
+def attn_host_inputs(w: AttentionWorkload, seed: int = 0):
+    """Q, K, V as bf16 bits, shaped (batch, rows, d); streams 0, 1, 2 of the seed."""
+    Q = inputs.bf16_matrix(w.batch * w.sq, w.d, w.dist, seed + inputs.STREAM_A).reshape(w.batch, w.sq, w.d)
+    K = inputs.bf16_matrix(w.batch * w.sk, w.d, w.dist, seed + inputs.STREAM_B).reshape(w.batch, w.sk, w.d)
+    V = inputs.bf16_matrix(w.batch * w.sk, w.d, w.dist, seed + inputs.STREAM_C).reshape(w.batch, w.sk, w.d)
+    return Q, K, V
+
+
+def attn_oracle_sample(w: AttentionWorkload, budget_s: float, seed: int = 0):
+    """Sizes and times an oracle sample: the first H heads, every query row against every key.
+
+    Returns (callable running the sample, TFLOP/s of one run, seconds, heads, threads).
+    """
+    import oracle
+    per_head = 4.0 * w.sq * w.sk * w.d
+
+    def head_inputs(h):
+        Q = inputs.bf16_matrix(h * w.sq, w.d, w.dist, seed + inputs.STREAM_A).reshape(h, w.sq, w.d)
+        K = inputs.bf16_matrix(h * w.sk, w.d, w.dist, seed + inputs.STREAM_B).reshape(h, w.sk, w.d)
+        V = inputs.bf16_matrix(h * w.sk, w.d, w.dist, seed + inputs.STREAM_C).reshape(h, w.sk, w.d)
+        return Q, K, V
+
+    Q, K, V = head_inputs(1)
+    t0 = time.perf_counter()
+    oracle.attention_forward(Q, K, V)
+    rate = per_head / max(time.perf_counter() - t0, 1e-6)
+    heads = max(1, min(w.batch, int(rate * budget_s / per_head)))
+    Q, K, V = head_inputs(heads)
+    t0 = time.perf_counter()
+    oracle.attention_forward(Q, K, V)
+    secs = time.perf_counter() - t0
+    return (lambda: oracle.attention_forward(Q, K, V)), heads * per_head / secs / 1e12, secs, heads, \
+        oracle.num_threads()
+
+
+def bench_attention_reference(args, w: AttentionWorkload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    per_step = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    run, _, _, heads, threads = attn_oracle_sample(w, per_step)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = 4.0 * heads * w.sq * w.sk * w.d * args.steps / total / 1e12
+    sample = f"heads 0..{heads - 1} (all {w.sq} query rows against all {w.sk} keys) per step, of the " \
+             f"{w.batch}-head workload"
+    line = {
+        "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "sq": w.sq, "sk": w.sk, "d": w.d,
+                   "description": "fp64 CPU oracle (softmax of the fp64 scores, OpenMP over rows): " + w.description},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_attention_ours(args, w: AttentionWorkload):
+    import numpy as np
+    import torch
+    world, rank, local = dist_env()
+    dist = init_dist(world, "nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from dense_gemm_cluster_gb300 import gemm
+    cluster = w.cluster if world == 1 else 1          # multicast stays off when several GPUs take part
+    Qh, Kh, Vh = attn_host_inputs(w)
+    Q = torch.from_numpy(Qh.reshape(-1).view(np.int16)).to(device)
+    K = torch.from_numpy(Kh.reshape(-1).view(np.int16)).to(device)
+    V = torch.from_numpy(Vh.reshape(-1).view(np.int16)).to(device)
+    odt = torch.float32 if w.out == "f32" else torch.int16
+    O = torch.empty(w.batch * w.sq * w.d, dtype=odt, device=device)
+    lse = torch.empty(w.batch * w.sq, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    out_f32 = 1 if w.out == "f32" else 0
+    launches = 0
+
+    def run():
+        nonlocal launches
+        s = gemm.attention_forward_run(Q, K, V, O, lse, w.batch, w.sq, w.sk, w.d, 0.0, out_f32, cluster, stream)
+        if s != gemm.GEMM_OK:
+            raise RuntimeError(f"attention_forward_run: status {s}")
+        launches += 1
+
+    for _ in range(max(3, args.warmup)):
+        run()
+    if gemm.attention_forward_query_status(stream) != gemm.GEMM_OK:
+        raise RuntimeError("attention kernel reported a device timeout")
+    input_bytes = w.min_hbm_bytes()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = launches
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            run()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - wall0
+    barrier(dist)
+    if gemm.attention_forward_query_status(stream) != gemm.GEMM_OK:
+        raise RuntimeError("attention kernel reported a device timeout")
+    local_s = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)) / 1e3
+    elapsed, units = aggregate(dist, local_s, float(w.flops) * args.steps, device)
+    peaks, peaks_kind = load_peaks()
+    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    avg_launch_s = local_s / args.steps
+    achieved = w.flops / avg_launch_s / 1e12
+    traffic_rec = recorded_traffic(w.name, ATTN_KERNEL_SOURCES)
+    line = {
+        "metric": ATTN_METRIC, "value": units / elapsed / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "sq": w.sq, "sk": w.sk, "d": w.d, "out": w.out,
+                   "cluster": cluster, "l2": f"no flush: the inputs ({input_bytes >> 20} MB) are larger than L2",
+                   "description": w.description},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tensor_peak, "peak_source": f"bf16_tflops (burst) of {peaks_kind}",
+                     "algorithmic_flops_per_launch": w.flops,
+                     "traffic": traffic_rec["dram_bytes"] if traffic_rec else None,
+                     "arithmetic_intensity": w.flops / w.min_hbm_bytes(),
+                     "ridge": tensor_peak * 1e12 / (hbm_peak * 1e9)},
+        "gpu_launches": launches - launches0,
+        "wall_s_timed_region": wall,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        line["e2e"] = attn_e2e(w, args, device, stream, dist, run, (Qh, Kh, Vh), (Q, K, V), (O, lse))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        _, rate, secs, heads, threads = attn_oracle_sample(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"heads 0..{heads - 1} of {w.batch} (all rows and keys) in {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def attn_e2e(w, args, device, stream, dist, run, host_in, dev_in, dev_out):
+    """The same metric with Q, K, V copied in from pinned host memory and O, lse copied out every step."""
+    import numpy as np
+    import torch
+    pinned = [torch.from_numpy(a.reshape(-1).view(np.int16)).pin_memory() for a in host_in]
+    O, lse = dev_out
+    O_h = torch.empty(O.numel(), dtype=O.dtype).pin_memory()
+    lse_h = torch.empty(lse.numel(), dtype=lse.dtype).pin_memory()
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def step():
+        for d_, h_ in zip(dev_in, pinned):
+            d_.copy_(h_, non_blocking=True)
+        run()
+        O_h.copy_(O, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        step()
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    local = time.perf_counter() - t0
+    elapsed, units = aggregate(dist, local, float(w.flops) * steps, device)
+    h2d = sum(int(h_.numel()) * 2 for h_ in pinned)
+    d2h = int(O_h.numel() * O_h.element_size() + lse_h.numel() * 4)
+    return {"value": units / elapsed / 1e12, "unit": "TFLOP/s", "steps": steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * elapsed / steps}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(ATTENTION_WORKLOADS), default=DEFAULT)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
@@ -471,6 +663,14 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload in ATTENTION_WORKLOADS:
+        w = ATTENTION_WORKLOADS[args.workload]
+        if args.batch:
+            import dataclasses
+            w = dataclasses.replace(w, batch=args.batch, name=f"{w.name}[batch={args.batch}]")
+        if args.impl == "reference":
+            return bench_attention_reference(args, w)
+        return bench_attention_ours(args, w)
     w = WORKLOADS[args.workload]
     if args.batch:
         import dataclasses

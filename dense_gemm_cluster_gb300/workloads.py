@@ -86,3 +86,35 @@ WORKLOADS = {
 }
 
 DEFAULT = "gemm4096_bf16_cluster2x1"
+
+
+@dataclass(frozen=True)
+class AttentionWorkload:
+    """Fused attention forward O = softmax(scale Q K^T) V over batch x heads independent heads."""
+    name: str
+    batch: int                      # batch x heads
+    sq: int
+    sk: int
+    d: int = 128
+    cluster: int = 2                # CTAs sharing each K/V tile by multicast
+    out: str = "bf16"
+    dist: str = "normal"
+    description: str = ""
+
+    @property
+    def flops(self) -> int:
+        return 4 * self.batch * self.sq * self.sk * self.d        # Q K^T and P V
+
+    def min_hbm_bytes(self) -> int:
+        """Q, K, V read once; O and the row log-sum-exp written once."""
+        esc = 4 if self.out == "f32" else 2
+        return self.batch * (2 * (self.sq + 2 * self.sk) * self.d + esc * self.sq * self.d + 4 * self.sq)
+
+
+ATTENTION_WORKLOADS = {
+    "attention_fwd_8x16x4096x4096x128": AttentionWorkload(
+        "attention_fwd_8x16x4096x4096x128", 128, 4096, 4096, cluster=2,
+        description="fused attention forward O = softmax(Q K^T / sqrt(128)) V with the row log-sum-exp, "
+                    "batch 8 x heads 16, seq 4096, head dim 128, N(0,1) bf16 Q/K/V, bf16 O, each K/V tile "
+                    "multicast across the 2 query-block CTAs of a cluster"),
+}
