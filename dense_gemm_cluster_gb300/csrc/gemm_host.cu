@@ -22,6 +22,8 @@ namespace {
 constexpr int kMaxSmemPerCta = 232448;        // 227 KB opt-in shared memory per block on sm_103
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int64_t kMinSplitBlocks = 16;         // k-blocks per cluster before a sub-wave problem is split wider
+constexpr double kMinTailUs = 4.0;              // saved last-wave time worth a stream-K split
+constexpr double kFlopPerUsPerSm = 1.5e9 / 152; // per-SM tensor rate for that estimate (1.5 PFLOP/s over 152 SMs)
 
 thread_local std::string g_thread_error;
 
@@ -176,13 +178,19 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
 }
 
 // Whole-tile waves and the stream-K tail for `tiles` cluster tiles on `clusters`
-// co-resident clusters. Returns the number of tiles processed whole (a multiple
-// of `clusters`); the rest are split by k-blocks.
-int64_t whole_tiles_for(int schedule, int64_t tiles, int64_t clusters, int num_kb, bool can_split) {
+// co-resident clusters of `cs` CTAs. Returns the number of tiles processed whole
+// (a multiple of `clusters`); the rest are split by k-blocks. The auto schedule
+// splits when that saves at least kMinTailUs: whole tiles take `waves` cluster-
+// tile times, an even split tiles / clusters of them, a cluster tile's time being
+// its FLOPs at cs SMs' share of the tensor rate. (Handing a partial to its
+// finisher costs a few microseconds, so a short tail is cheaper left idle.)
+int64_t whole_tiles_for(int schedule, int64_t tiles, int64_t clusters, int num_kb, bool can_split, double flops,
+                        int cs) {
     if (!can_split || schedule == 1 || schedule == 3 || num_kb < 2 || tiles == 0 || clusters <= 1) return tiles;
     const int64_t waves = (tiles + clusters - 1) / clusters;
-    const double fill = (double)tiles / (double)(waves * clusters);
-    if (schedule == 0 && fill >= 0.9) return tiles;
+    const double tile_us = flops / (double)tiles / (kFlopPerUsPerSm * cs);
+    const double saved_us = ((double)waves - (double)tiles / (double)clusters) * tile_us;
+    if (schedule == 0 && saved_us < kMinTailUs) return tiles;
     const int64_t full = tiles / clusters;
     return (full > 0 ? full - 1 : 0) * clusters;
 }
@@ -279,7 +287,9 @@ extern "C" gemm_status_t gemm_plan(const gemm_options_t* opt, int64_t M, int64_t
     if (s == GEMM_OK) {
         *plan = r.pub;
         const int num_kb = (int)ceil_div(K, r.pub.block_k);
-        plan->stream_k_tiles = r.pub.tiles - whole_tiles_for(opt->schedule, r.pub.tiles, r.pub.clusters, num_kb, true);
+        plan->stream_k_tiles = r.pub.tiles - whole_tiles_for(opt->schedule, r.pub.tiles, r.pub.clusters, num_kb, true,
+                                                             2.0 * (double)M * (double)N * (double)K * (double)batch,
+                                                             r.pub.cluster_m * r.pub.cluster_n);
     }
     return s;
 }
@@ -587,7 +597,8 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     // Stream-K tail (needs the co-residency the occupancy cap guarantees, and a workspace).
     if (o.schedule == 2 && h->no_alloc)
         return fail(&h->err, GEMM_ERR_UNSUPPORTED, "the stream-K tail needs a workspace; gemm_run_noalloc runs whole tiles");
-    kp.dp_tiles = whole_tiles_for(o.schedule, pl.tiles, clusters, kp.num_kb, !h->no_alloc);
+    kp.dp_tiles = whole_tiles_for(o.schedule, pl.tiles, clusters, kp.num_kb, !h->no_alloc,
+                                  2.0 * (double)M * (double)N * (double)K * (double)batch, cs);
     kp.sk_iters = (pl.tiles - kp.dp_tiles) * kp.num_kb;
     if (kp.sk_iters == 0 && o.schedule != 3 && clusters > pl.tiles) clusters = pl.tiles;   // whole tiles only
     cfg.gridDim = dim3((unsigned)(clusters * cs), 1, 1);
