@@ -104,3 +104,23 @@ def test_attention_row_max_sees_every_column():
         vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
         assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
         assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+
+
+def test_attention_more_query_blocks_than_sms():
+    # 320 CTAs (160 heads x 2 query blocks, one ragged) on 152 SMs, ragged key tiles
+    # and rescales of the reference max; clusters of 2 and 4 must equal cluster 1.
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    Q, K, V = _inputs(160, 300, 640, 41, k_growth=2.0)
+    ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True)
+    vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+    base = None
+    for cluster in (1, 2, 4):
+        o, lse = _run(Q, K, V, cluster, out_f32=1)
+        assert np.isfinite(o).all()
+        assert np.max(np.abs(o - ref)) <= 1e-2 * vmax, f"cluster {cluster}"
+        assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+        if base is None:
+            base = (o, lse)
+        else:
+            assert np.array_equal(o, base[0]) and np.array_equal(lse, base[1])
