@@ -538,6 +538,7 @@ def bench_attention_ours(args, w: AttentionWorkload):
     torch.cuda.set_device(device)
     from dense_gemm_cluster_gb300 import gemm
     cluster = w.cluster if world == 1 else 1          # multicast stays off when several GPUs take part
+    cta_group = w.cta_group if world == 1 else 1
     Qh, Kh, Vh = attn_host_inputs(w)
     Q = torch.from_numpy(Qh.reshape(-1).view(np.int16)).to(device)
     K = torch.from_numpy(Kh.reshape(-1).view(np.int16)).to(device)
@@ -551,7 +552,8 @@ def bench_attention_ours(args, w: AttentionWorkload):
 
     def run():
         nonlocal launches
-        s = gemm.attention_forward_run(Q, K, V, O, lse, w.batch, w.sq, w.sk, w.d, 0.0, out_f32, cluster, stream)
+        s = gemm.attention_forward_run(Q, K, V, O, lse, w.batch, w.sq, w.sk, w.d, 0.0, out_f32, cluster,
+                                       cta_group=cta_group, stream=stream)
         if s != gemm.GEMM_OK:
             raise RuntimeError(f"attention_forward_run: status {s}")
         launches += 1
@@ -590,7 +592,8 @@ def bench_attention_ours(args, w: AttentionWorkload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "sq": w.sq, "sk": w.sk, "d": w.d, "out": w.out,
-                   "cluster": cluster, "l2": f"no flush: the inputs ({input_bytes >> 20} MB) are larger than L2",
+                   "cluster": cluster, "cta_group": cta_group,
+                   "l2": f"no flush: the inputs ({input_bytes >> 20} MB) are larger than L2",
                    "description": w.description},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
                      "frac": achieved / tensor_peak, "peak_source": f"bf16_tflops (burst) of {peaks_kind}",

@@ -24,6 +24,15 @@
 //               per thread, online softmax in base 2 with a reference max that
 //               moves (rescaling O in TMEM) only when the row max grows by
 //               more than 2^8; at the end O / l and the log-sum-exp.
+//
+// Pair mode ("Clusters, distributed shared memory & cluster launch control",
+// section "Two CTAs, one MMA"): a 2-CTA cluster issues tcgen05.mma.cta_group::2
+// from its even CTA. S_i = Q_i K_j^T runs as one M = 256 MMA over both CTAs'
+// Q_i (each CTA's scores land in its own TMEM), each CTA holding half of every
+// K tile (64 keys) and half of every V tile (64 of the d columns), so per SM
+// the score MMA reads 6 KB of shared memory per K step instead of 8 and P V
+// 2 KB instead of 4. The odd CTA's softmax warps hand P back to the even CTA's
+// barrier; completions are multicast to both CTAs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -49,7 +58,7 @@ constexpr uint32_t TILE_BYTES = 128 * HD * 2;   // 32 KB: a Q, K or V tile
 constexpr uint32_t ATOM_BYTES = 128 * 128;      // one 64-element swizzle atom of a 128-row tile
 constexpr int NS = 4;                           // ring slots; K and V tiles alternate
 constexpr float RESCALE_THRESHOLD = 8.0f;       // log2 units: move the reference max past 2^8 growth
-constexpr size_t SMEM_BYTES = 1024 + (QT + NS) * TILE_BYTES + 16 * 8 + 16;
+constexpr size_t SMEM_BYTES = 1024 + (QT + NS) * TILE_BYTES + 24 * 8 + 16;
 
 __device__ unsigned int g_attn_status[4];
 
@@ -81,23 +90,61 @@ __device__ bool attn_wait(uint32_t bar, uint32_t parity, const AttnParams& p, ui
     }
 }
 
+// The same wait with a cluster-scope acquire: for barriers a peer CTA arrives on
+// with a release (the pair's odd CTA handing its P to the even CTA).
+__device__ bool attn_wait_cluster(uint32_t bar, uint32_t parity, const AttnParams& p, uint32_t code) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t c0 = clock_cycles();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (clock_cycles() - c0 > 2ull * p.timeout_ns) {
+            if (atomicCAS(&g_attn_status[0], 0u, code) == 0u) {
+                g_attn_status[1] = blockIdx.x;
+                g_attn_status[2] = blockIdx.y;
+                __threadfence();
+            }
+            return false;
+        }
+    }
+}
+
+// O (+)= P V as one pair MMA: P (packed bf16) from TMEM of both CTAs of the pair.
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // K-major 128-row tile as an MMA operand: atoms of 64 elements are 16 KB apart.
 __device__ __forceinline__ uint32_t kmajor_koff(int k) { return (uint32_t)((k >> 2) * ATOM_BYTES + (k & 3) * 32) >> 4; }
+// Half a K tile (64 keys) in pair mode: atoms 8 KB apart.
+__device__ __forceinline__ uint32_t kmajor_koff_half(int k) {
+    return (uint32_t)((k >> 2) * (ATOM_BYTES / 2) + (k & 3) * 32) >> 4;
+}
 // MN-major tile (V: 128 keys x 128 d): K step of 16 keys = 16 rows of 128 bytes.
 __device__ __forceinline__ uint32_t mnmajor_koff(int k) { return (uint32_t)(k * 2048) >> 4; }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    // Ring: NS slots of a whole K or V tile, or (pair) twice as many of half tiles.
+    constexpr int NSL = PAIR ? 2 * NS : NS;
+    constexpr uint32_t SLOT_BYTES = PAIR ? TILE_BYTES / 2 : TILE_BYTES;
+    constexpr int G = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                                   // QT tiles
     uint8_t* ring = sQ + QT * TILE_BYTES;                 // NS slots
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + NS * TILE_BYTES);
     uint64_t* q_full = bars;                 // 1
-    uint64_t* kv_full = bars + 1;            // NS
-    uint64_t* kv_empty = bars + 1 + NS;      // NS
-    uint64_t* s_full = bars + 1 + 2 * NS;    // QT: S_i written
+    uint64_t* kv_full = bars + 1;            // NSL
+    uint64_t* kv_empty = bars + 1 + NSL;     // NSL
+    uint64_t* s_full = bars + 1 + 2 * NSL;   // QT: S_i written
     uint64_t* p_full = s_full + QT;          // QT: P_i written (and O_i rescaled)
     uint64_t* pv_done = p_full + QT;         // QT: O_i += P_i V_j completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pv_done + QT);
@@ -110,21 +157,23 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int q0 = blockIdx.x * (QT * TQ);
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(q_full), 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(smem_u32(&kv_full[s]), (uint32_t)c);    // one arm per issuer of a slice
-            mbar_init(smem_u32(&kv_empty[s]), (uint32_t)c);   // one release per consumer CTA
+        // Pair: the even CTA's q_full and kv_full count both CTAs' arms and bytes, its
+        // p_full both CTAs' softmax warps; every release and completion is multicast.
+        mbar_init(smem_u32(q_full), PAIR ? 2u : 1u);
+        for (int s = 0; s < NSL; ++s) {
+            mbar_init(smem_u32(&kv_full[s]), PAIR ? 2u : (uint32_t)c);    // one arm per issuer of a slice
+            mbar_init(smem_u32(&kv_empty[s]), PAIR ? 1u : (uint32_t)c);   // one release per consumer CTA
         }
         for (int i = 0; i < QT; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&p_full[i]), 4);
+            mbar_init(smem_u32(&p_full[i]), PAIR ? 8u : 4u);
             mbar_init(smem_u32(&pv_done[i]), 1);
         }
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_u32(tmem_slot), 512);
-        tmem_relinquish<1>();
+        tmem_alloc<G>(smem_u32(tmem_slot), 512);
+        tmem_relinquish<G>();
     }
     tc_fence_before();
     __syncthreads();
@@ -132,7 +181,82 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;        // columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512)
 
-    if (warp == 0 && lane == 0) {
+    if (PAIR && warp == 0 && lane == 0) {
+        // ---------------------------------------------------------------- producer (pair)
+        // This CTA's Q tiles and its half of each K tile (64 keys) and V tile (64 of the
+        // d columns), each arming and signalling the even CTA's barrier.
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        const uint32_t leader = rank & ~1u;
+        const int h = (int)(rank & 1u);
+        const uint32_t qb = mapa(smem_u32(q_full), leader);
+        mbar_arrive_expect_tx_cluster(qb, QT * TILE_BYTES);
+        for (int i = 0; i < QT; ++i)
+            tma_load_4d_pair(smem_u32(sQ + i * TILE_BYTES), &tmQ, qb, 0, q0 + i * TQ, 0, b);
+        const int loads = 2 * p.n_kv;
+        for (int n = 0; n < loads; ++n) {
+            const int s = n % NSL;
+            const uint32_t ph = (uint32_t)(n / NSL) & 1u;
+            if (!attn_wait(smem_u32(&kv_empty[s]), ph ^ 1u, p, 1)) break;
+            const uint32_t fb = mapa(smem_u32(&kv_full[s]), leader);
+            mbar_arrive_expect_tx_cluster(fb, SLOT_BYTES);
+            const uint32_t dst = smem_u32(ring + s * SLOT_BYTES);
+            const int key0 = (n >> 1) * TK;
+            if ((n & 1) == 0) tma_load_4d_pair(dst, &tmK, fb, 0, key0 + h * (TK / 2), 0, b);
+            else              tma_load_3d_pair(dst, &tmV, fb, h * 64, key0, b);
+        }
+        // Every slot this thread filled is released before exit.
+        for (int n = loads; n < loads + NSL; ++n) {
+            const int s = n % NSL;
+            if (!attn_wait(smem_u32(&kv_empty[s]), ((uint32_t)(n / NSL) & 1u) ^ 1u, p, 1)) break;
+        }
+    } else if (PAIR && warp == 1 && lane == 0) {
+        // ---------------------------------------------------------------- MMA issuer (pair)
+        // Only the even CTA issues; the order matches the single-CTA kernel below.
+        if ((rank & 1u) == 0) {
+            const uint16_t pairm = (uint16_t)(3u << rank);
+            const uint32_t idesc_s = instr_desc_bf16(2 * TQ, TK, false, false);
+            const uint32_t idesc_o = instr_desc_bf16(2 * TQ, HD, false, true);
+            const uint64_t ring_k = smem_desc_sw128(smem_u32(ring), false, 0);
+            const uint64_t ring_v = smem_desc_sw128(smem_u32(ring), true, SLOT_BYTES);
+            bool ok = attn_wait(smem_u32(q_full), 0, p, 2);
+            auto issue_s = [&](int i, int j) -> bool {
+                const int n = 2 * j, s = n % NSL;
+                if (i == 0) {
+                    if (!attn_wait(smem_u32(&kv_full[s]), (uint32_t)(n / NSL) & 1u, p, 3)) return false;
+                    tc_fence_after();
+                }
+                const uint64_t dq = smem_desc_sw128(smem_u32(sQ + i * TILE_BYTES), false, 0);
+                const uint64_t dk = ring_k + ((s * SLOT_BYTES) >> 4);
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k)
+                    mma_bf16<2>(tmem + i * TK, dq + kmajor_koff(k), dk + kmajor_koff_half(k), idesc_s, k > 0 ? 1u : 0u);
+                mma_commit_mcast<2>(smem_u32(&s_full[i]), pairm);
+                if (i == QT - 1) mma_commit_mcast<2>(smem_u32(&kv_empty[s]), pairm);
+                return true;
+            };
+            auto issue_pv = [&](int i, int j) -> bool {
+                const int n = 2 * j + 1, s = n % NSL;
+                if (i == 0 && !attn_wait(smem_u32(&kv_full[s]), (uint32_t)(n / NSL) & 1u, p, 4)) return false;
+                if (!attn_wait_cluster(smem_u32(&p_full[i]), (uint32_t)j & 1u, p, 5)) return false;
+                tc_fence_after();
+                const uint64_t dv = ring_v + ((s * SLOT_BYTES) >> 4);
+#pragma unroll
+                for (int k = 0; k < TK / 16; ++k)
+                    mma_bf16_ts_pair(tmem + 2 * TK + i * HD, tmem + i * TK + k * 8, dv + mnmajor_koff(k), idesc_o,
+                                     (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit_mcast<2>(smem_u32(&pv_done[i]), pairm);
+                if (i == QT - 1) mma_commit_mcast<2>(smem_u32(&kv_empty[s]), pairm);
+                return true;
+            };
+            if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
+            for (int j = 0; ok && j < p.n_kv; ++j) {
+                const bool more = j + 1 < p.n_kv;
+                ok = issue_pv(0, j) && (!more || issue_s(0, j + 1)) && issue_pv(1, j) && (!more || issue_s(1, j + 1));
+            }
+        }
+    } else if (!PAIR && warp == 0 && lane == 0) {
         // ---------------------------------------------------------------- producer
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
@@ -177,7 +301,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int s = n % NS;
             if (!attn_wait(smem_u32(&kv_empty[s]), ((uint32_t)(n / NS) & 1u) ^ 1u, p, 1)) break;
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (!PAIR && warp == 1 && lane == 0) {
         // ---------------------------------------------------------------- MMA issuer
         const uint32_t idesc_s = instr_desc_bf16(TQ, TK, false, false);    // Q (K-major) x K^T (K-major)
         const uint32_t idesc_o = instr_desc_bf16(TQ, HD, false, true);     // P (TMEM) x V (MN-major)
@@ -311,7 +435,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_local(smem_u32(&p_full[ti]));
+            if (lane == 0) {
+                // The pair's odd CTA hands its P to the even CTA's barrier with a
+                // cluster-scope release (the even CTA's MMAs read this CTA's TMEM).
+                if (!PAIR || (rank & 1u) == 0) mbar_arrive_local(smem_u32(&p_full[ti]));
+                else                           mbar_arrive_cluster(mapa(smem_u32(&p_full[ti]), rank & ~1u));
+            }
         }
         // Final normalisation: O / l, and lse = (m_ref + log2 l) * ln 2.
         if (ok && attn_wait(smem_u32(&pv_done[ti]), (uint32_t)(p.n_kv - 1) & 1u, p, 9)) {
@@ -350,7 +479,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     if (c > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<1>(tmem, 512);
+        tmem_dealloc<G>(tmem, 512);
     }
 }
 
@@ -385,12 +514,15 @@ bool encode(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* p
 
 extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, const void* V, void* O, float* lse,
                                                int64_t batch, int64_t sq, int64_t sk, int64_t d, float scale,
-                                               int out_f32, int cluster, void* stream) {
+                                               int out_f32, int cluster, int cta_group, void* stream) {
     if (batch < 0 || sq < 0 || sk < 0) return afail(GEMM_ERR_INVALID_ARG, "negative size");
     if (batch == 0 || sq == 0) return GEMM_OK;
     if (sk == 0) return afail(GEMM_ERR_INVALID_ARG, "sk must be at least 1");
     if (d != HD) return afail(GEMM_ERR_UNSUPPORTED, "head dimension must be 128");
     if (cluster != 1 && cluster != 2 && cluster != 4) return afail(GEMM_ERR_UNSUPPORTED, "cluster must be 1, 2 or 4");
+    if (cta_group != 1 && cta_group != 2) return afail(GEMM_ERR_UNSUPPORTED, "cta_group must be 1 or 2");
+    if (cta_group == 2 && cluster != 2) return afail(GEMM_ERR_UNSUPPORTED, "the pair MMA runs in clusters of 2");
+    const bool pair = cta_group == 2;
     if (!Q || !K || !V || !O) return afail(GEMM_ERR_INVALID_ARG, "null pointer");
     if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
          reinterpret_cast<uintptr_t>(O) | reinterpret_cast<uintptr_t>(lse)) & 15u)
@@ -405,12 +537,14 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     const cuuint32_t qb[4] = {64, TQ, 2, 1};
     const cuuint64_t kd[4] = {64, (cuuint64_t)sk, 2, (cuuint64_t)batch};
     const cuuint64_t ks[3] = {HD * 2, 128, (cuuint64_t)(sk * HD * 2)};
-    // A K slice: whole atoms first (cluster <= 2), then half the rows of one atom (cluster 4).
-    const cuuint32_t kb[4] = {64, (cuuint32_t)(cluster <= 2 ? TK : TK / 2), (cuuint32_t)(cluster == 1 ? 2 : 1), 1};
-    // V: MN-major boxes of 64 d columns x (128 / cluster) keys.
+    // A K slice: whole atoms first (cluster <= 2), then half the rows of one atom (cluster 4);
+    // pair mode: half the keys, both atoms.
+    const cuuint32_t kb[4] = {64, (cuuint32_t)(pair ? TK / 2 : (cluster <= 2 ? TK : TK / 2)),
+                              (cuuint32_t)(pair || cluster == 1 ? 2 : 1), 1};
+    // V: MN-major boxes of 64 d columns x (128 / cluster) keys (pair mode: all 128 keys).
     const cuuint64_t vd[3] = {HD, (cuuint64_t)sk, (cuuint64_t)batch};
     const cuuint64_t vs[2] = {HD * 2, (cuuint64_t)(sk * HD * 2)};
-    const cuuint32_t vb[3] = {64, (cuuint32_t)(TK / cluster), 1};
+    const cuuint32_t vb[3] = {64, (cuuint32_t)(pair ? TK : TK / cluster), 1};
     if (!encode(enc, &tq, Q, 4, qd, qs, qb) || !encode(enc, &tk, K, 4, kd, ks, kb) || !encode(enc, &tv, V, 3, vd, vs, vb))
         return afail(GEMM_ERR_INVALID_ARG, "tensor map encode failed");
     AttnParams p;
@@ -425,7 +559,8 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     p.out = O;
     p.lse = lse;
     p.timeout_ns = 2000000000ull;
-    void* fn = reinterpret_cast<void*>(&attention_fwd_kernel);
+    void* fn = pair ? reinterpret_cast<void*>(&attention_fwd_kernel<true>)
+                    : reinterpret_cast<void*>(&attention_fwd_kernel<false>);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));
     long long ctas = (sq + QT * TQ - 1) / (QT * TQ);

@@ -293,15 +293,16 @@ def stencil_1d_query_status(stream=None) -> int:
 
 
 # ---------------------------------------------------------------- fused attention forward (include/attention.h)
-_lib.attention_forward_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _i32, _vp]
+_lib.attention_forward_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _i32, _i32, _vp]
 _lib.attention_forward_run.restype = _i32
 _lib.attention_forward_query_status.argtypes = [_vp]
 _lib.attention_forward_query_status.restype = _i32
 
 
-def attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, scale=0.0, out_f32=0, cluster=1, stream=None) -> int:
+def attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, scale=0.0, out_f32=0, cluster=1, cta_group=1,
+                          stream=None) -> int:
     return _lib.attention_forward_run(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), batch, sq, sk, d, scale,
-                                      out_f32, cluster, _stream(stream))
+                                      out_f32, cluster, cta_group, _stream(stream))
 
 
 def attention_forward_query_status(stream=None) -> int:

@@ -96,7 +96,8 @@ class AttentionWorkload:
     sq: int
     sk: int
     d: int = 128
-    cluster: int = 2                # CTAs sharing each K/V tile by multicast
+    cluster: int = 2                # CTAs sharing each K/V tile
+    cta_group: int = 1              # 1: multicast of whole K/V tiles; 2: pair MMA over half tiles
     out: str = "bf16"
     dist: str = "normal"
     description: str = ""

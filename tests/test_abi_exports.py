@@ -161,3 +161,22 @@ def test_plan_sub_wave_spread(lib):
     assert p.clusters == 6 and p.stream_k_tiles == 0
     s, p = plan(lib, 256, 256, 256, sm=152, mode="mcast", mcast_b=1, cluster_m=2)
     assert p.tiles == 1 and p.clusters == 1
+
+
+def test_attention_validation_before_launch(lib):
+    # Every one of these returns before any CUDA call (no GPU needed); the fake device
+    # addresses are never dereferenced.
+    a, m = 1 << 20, (1 << 20) + 2                # 16-byte aligned / misaligned fake addresses
+    run = lib.attention_forward_run
+    assert run(a, a, a, a, None, 1, 128, 128, 64) == lib.GEMM_ERR_UNSUPPORTED          # head dim
+    assert run(a, a, a, a, None, 1, 128, 128, 128, 0.0, 0, 3) == lib.GEMM_ERR_UNSUPPORTED
+    assert run(a, a, a, a, None, 1, 128, 128, 128, 0.0, 0, 4, 2) == lib.GEMM_ERR_UNSUPPORTED         # pair needs 2
+    assert run(a, a, a, a, None, 1, 128, 128, 128, 0.0, 0, 2, 3) == lib.GEMM_ERR_UNSUPPORTED
+    assert run(a, a, a, a, None, 1, 128, 0, 128) == lib.GEMM_ERR_INVALID_ARG              # no keys
+    assert run(a, a, a, a, None, -1, 128, 128, 128) == lib.GEMM_ERR_INVALID_ARG
+    assert run(None, a, a, a, None, 1, 128, 128, 128) == lib.GEMM_ERR_INVALID_ARG
+    assert run(m, a, a, a, None, 1, 128, 128, 128) == lib.GEMM_ERR_ALIGNMENT
+    assert run(a, a, a, a, m, 1, 128, 128, 128) == lib.GEMM_ERR_ALIGNMENT               # lse
+    assert run(a, a, a, a, None, 1 << 16, 128, 128, 128) == lib.GEMM_ERR_INVALID_ARG      # batch limit
+    assert run(a, a, a, a, None, 0, 128, 128, 128) == lib.GEMM_OK                         # nothing to do
+    assert run(a, a, a, a, None, 3, 0, 128, 128) == lib.GEMM_OK

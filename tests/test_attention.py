@@ -24,7 +24,7 @@ def _inputs(b, sq, sk, seed, k_growth=0.0):
     return Q, K, V
 
 
-def _run(Q, K, V, cluster, out_f32=0, scale=0.0):
+def _run(Q, K, V, cluster, out_f32=0, scale=0.0, cta_group=1):
     import torch
     from dense_gemm_cluster_gb300 import gemm
     b, sq, _ = Q.shape
@@ -32,20 +32,23 @@ def _run(Q, K, V, cluster, out_f32=0, scale=0.0):
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
     O = torch.full((b * sq * 128,), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
     lse = torch.full((b * sq,), float("nan"), dtype=torch.float32, device="cuda")
-    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, 128, scale, out_f32, cluster)
+    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, 128, scale, out_f32, cluster, cta_group)
     assert s == gemm.GEMM_OK
     assert gemm.attention_forward_query_status() == gemm.GEMM_OK
     o = O.float().cpu().numpy().reshape(b, sq, 128).astype(np.float64)
     return o, lse.cpu().numpy().reshape(b, sq).astype(np.float64)
 
 
+MODES = [(1, 1), (2, 1), (4, 1), (2, 2)]          # (cluster, cta_group)
+
+
 @pytest.mark.parametrize("b,sq,sk", [(2, 128, 128), (3, 300, 500), (1, 1000, 130), (2, 256, 2048), (1, 77, 1)])
-@pytest.mark.parametrize("cluster", [1, 2, 4])
-def test_attention_matches_oracle(b, sq, sk, cluster):
+@pytest.mark.parametrize("cluster,cta_group", MODES)
+def test_attention_matches_oracle(b, sq, sk, cluster, cta_group):
     import oracle
     from dense_gemm_cluster_gb300 import inputs
     Q, K, V = _inputs(b, sq, sk, 100 + sq)
-    o, lse = _run(Q, K, V, cluster)
+    o, lse = _run(Q, K, V, cluster, cta_group=cta_group)
     ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True)
     vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
     assert np.isfinite(o).all()
@@ -53,24 +56,27 @@ def test_attention_matches_oracle(b, sq, sk, cluster):
     assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
 
 
-def test_attention_rescales_when_the_row_max_grows():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_attention_rescales_when_the_row_max_grows(cta_group):
     import oracle
     from dense_gemm_cluster_gb300 import inputs
     Q, K, V = _inputs(2, 256, 1024, 7, k_growth=3.0)
     for scale in (0.0, 0.35):
-        o, lse = _run(Q, K, V, 2, out_f32=1, scale=scale)
+        o, lse = _run(Q, K, V, 2, out_f32=1, scale=scale, cta_group=cta_group)
         ref, ref_lse = oracle.attention_forward(Q, K, V, scale=scale if scale else None, with_lse=True)
         vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
         assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
         assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
 
 
-def test_attention_multicast_is_bit_identical():
+def test_attention_sharing_modes_are_bit_identical():
+    # multicast only moves data; the pair MMA splits each 256-row product across two SMs
+    # but sums the same products in the same order
     Q, K, V = _inputs(2, 512, 640, 9)
     base, base_lse = _run(Q, K, V, 1, out_f32=1)
-    for c in (2, 4):
-        o, lse = _run(Q, K, V, c, out_f32=1)
-        assert np.array_equal(o, base) and np.array_equal(lse, base_lse)
+    for c, g in MODES[1:]:
+        o, lse = _run(Q, K, V, c, out_f32=1, cta_group=g)
+        assert np.array_equal(o, base) and np.array_equal(lse, base_lse), (c, g)
 
 
 def test_attention_argument_errors():
@@ -79,6 +85,8 @@ def test_attention_argument_errors():
     x = torch.zeros(128 * 128, dtype=torch.int16, device="cuda")
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 64) == gemm.GEMM_ERR_UNSUPPORTED
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 3) == gemm.GEMM_ERR_UNSUPPORTED
+    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 4, 2) == gemm.GEMM_ERR_UNSUPPORTED
+    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 2, 3) == gemm.GEMM_ERR_UNSUPPORTED
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 0, 128) == gemm.GEMM_ERR_INVALID_ARG
     assert gemm.attention_forward_run(x.data_ptr() + 2, x, x, x, None, 1, 128, 128, 128) == gemm.GEMM_ERR_ALIGNMENT
 
@@ -97,8 +105,8 @@ def test_attention_row_max_sees_every_column():
     Q = inputs.f64_to_bf16_bits(eye(sq) + noise(sq, 31)).reshape(b, sq, d)
     K = inputs.f64_to_bf16_bits(eye(sk) + noise(sk, 32)).reshape(b, sk, d)
     V = inputs.bf16_matrix(sk, d, "normal", 33).reshape(b, sk, d)
-    for cluster in (1, 2):
-        o, lse = _run(Q, K, V, cluster, out_f32=1, scale=1.0)
+    for cluster, g in ((1, 1), (2, 1), (2, 2)):
+        o, lse = _run(Q, K, V, cluster, out_f32=1, scale=1.0, cta_group=g)
         ref, ref_lse = oracle.attention_forward(Q, K, V, scale=1.0, with_lse=True)
         assert np.isfinite(o).all() and np.isfinite(lse).all()
         vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
@@ -115,10 +123,10 @@ def test_attention_more_query_blocks_than_sms():
     ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True)
     vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
     base = None
-    for cluster in (1, 2, 4):
-        o, lse = _run(Q, K, V, cluster, out_f32=1)
+    for cluster, g in MODES:
+        o, lse = _run(Q, K, V, cluster, out_f32=1, cta_group=g)
         assert np.isfinite(o).all()
-        assert np.max(np.abs(o - ref)) <= 1e-2 * vmax, f"cluster {cluster}"
+        assert np.max(np.abs(o - ref)) <= 1e-2 * vmax, f"cluster {cluster} cta_group {g}"
         assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
         if base is None:
             base = (o, lse)

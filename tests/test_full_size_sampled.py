@@ -101,7 +101,8 @@ def test_attention_workload_full_size_sampled():
     dev = lambda a: torch.from_numpy(a.reshape(-1).view(np.int16)).cuda()
     O = torch.empty(w.batch * w.sq * w.d, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(w.batch * w.sq, dtype=torch.float32, device="cuda")
-    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, w.batch, w.sq, w.sk, w.d, 0.0, 0, w.cluster)
+    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, w.batch, w.sq, w.sk, w.d, 0.0, 0, w.cluster,
+                                   w.cta_group)
     assert s == gemm.GEMM_OK and gemm.attention_forward_query_status() == gemm.GEMM_OK
     O = O.view(w.batch, w.sq, w.d)
     lse = lse.view(w.batch, w.sq)
