@@ -1,11 +1,12 @@
 """Runs the TMA unicast / multicast load microbenchmark (include/tma_bench.h).
 
-    python -m dense_gemm_cluster_gb300.tma_bench [--sweep]
+    python -m dense_gemm_cluster_gb300.tma_bench [--sweep] [--scenario l2|dram] [--mode M]
 
 Default: the two scenarios of "Hopper TMA Multicast 深度解析与实测", section
 实机运行与 NCU 验证 (a 4096 x 4096 bf16 matrix, 128 x 64 tiles, 2-CTA
 clusters, 5000 loads per CTA; L2 reuse and DRAM streaming), unicast against
-multicast, rewritten for sm_103a with a pipelined ring of loads. ``--sweep``
+multicast, rewritten for sm_103a with a pipelined ring of loads;
+``--scenario`` / ``--mode`` run one of them alone (for profiling). ``--sweep``
 varies the tile height, the ring depth and the cluster size. One JSON line per
 run: time, delivered and issued bytes, delivered GB/s, bytes per SM cycle.
 """
@@ -60,6 +61,8 @@ def run(mode="unicast", cluster=2, box_rows=128, stages=4, iters=5000, warmup=50
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--scenario", choices=("l2", "dram"), default=None, help="one scenario (default: both)")
+    ap.add_argument("--mode", choices=sorted(MODES), default=None, help="one mode (default: unicast, multicast)")
     args = ap.parse_args(argv)
     import torch
     dev = torch.device("cuda", 0)
@@ -67,11 +70,14 @@ def main(argv=None):
     src = (torch.arange(rows * cols, device=dev, dtype=torch.int32) % 65521).to(torch.int16)
     big = None
     if not args.sweep:
-        for stride, label in ((0, "L2 reuse"), (1, "DRAM streaming")):
+        big_rows = 131072                      # 1 GiB of bf16: larger than L2
+        scenarios = ((0, "L2 reuse"), (1, "DRAM streaming"))
+        if args.scenario:
+            scenarios = scenarios[:1] if args.scenario == "l2" else scenarios[1:]
+        for stride, label in scenarios:
             if stride:
-                big_rows = 131072              # 1 GiB of bf16: larger than L2
                 big = (torch.arange(big_rows * cols, device=dev, dtype=torch.int32) % 65521).to(torch.int16)
-            for mode in ("unicast", "multicast"):
+            for mode in ((args.mode,) if args.mode else ("unicast", "multicast")):
                 r = run(mode, 2, 128, 4, 5000, 50, stride, rows=big_rows if stride else rows, cols=cols,
                         src=big if stride else src)
                 r["scenario"] = label
