@@ -50,12 +50,30 @@ __device__ bool bench_wait(uint32_t bar, uint32_t parity, const BenchParams& p, 
     }
 }
 
-__device__ __forceinline__ void tile_origin(const BenchParams& p, int it, uint32_t cid, uint32_t ncl,
-                                            int& x, int& y) {
-    const long long ntiles = (long long)p.tiles_x * p.tiles_y;
-    const long long t = ((long long)it * p.stride * ncl + cid) % ntiles;
-    x = (int)(t % p.tiles_x) * 64;
-    y = (int)(t / p.tiles_x) * p.box_rows;
+// Tile of iteration `it`: (it * stride * clusters + cluster id) mod tiles, walked
+// incrementally (one conditional subtraction per load instead of a 64-bit
+// division, which would cost the issuing thread more than the load itself).
+struct TileWalk {
+    long long t, step, ntiles;
+    __device__ void init(const BenchParams& p, uint32_t cid, uint32_t ncl) {
+        ntiles = (long long)p.tiles_x * p.tiles_y;
+        t = (long long)cid % ntiles;
+        step = ((long long)p.stride * ncl) % ntiles;
+    }
+    __device__ void next() {
+        t += step;
+        if (t >= ntiles) t -= ntiles;
+    }
+    __device__ void origin(const BenchParams& p, int& x, int& y) const {
+        x = (int)(t % p.tiles_x) * 64;
+        y = (int)(t / p.tiles_x) * p.box_rows;
+    }
+};
+
+// Release of a slot the consumer did not read: ordering nothing, a relaxed
+// arrive avoids the memory barrier a release at cluster scope costs.
+__device__ __forceinline__ void arrive_relaxed_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
 }
 
 __global__ void __launch_bounds__(64, 1)
@@ -94,12 +112,14 @@ tma_bench_kernel(const __grid_constant__ CUtensorMap tm, const BenchParams p) {
             prefetch_tmap(&tm);
             const int slice_rows = p.mode == TMA_BENCH_MULTICAST_SLICED ? p.box_rows / (int)c : p.box_rows;
             const uint32_t slice_bytes = (uint32_t)slice_rows * 128u;
-            for (int it = 0; ok && it < total; ++it) {
-                const int slot = it % S;
-                const uint32_t phase = (uint32_t)(it / S) & 1u;
+            TileWalk tw;
+            tw.init(p, cid, ncl);
+            int slot = 0;
+            uint32_t phase = 0;
+            for (int it = 0; ok && it < total; ++it, tw.next()) {
                 if (!bench_wait(smem_u32(&empty[slot]), phase ^ 1u, p, 1)) { ok = false; break; }
                 int x, y;
-                tile_origin(p, it, cid, ncl, x, y);
+                tw.origin(p, x, y);
                 const uint32_t fb = smem_u32(&full[slot]);
                 const uint32_t dst = smem_u32(smem + slot * box_bytes);
                 if (p.mode == TMA_BENCH_UNICAST) {
@@ -117,6 +137,7 @@ tma_bench_kernel(const __grid_constant__ CUtensorMap tm, const BenchParams p) {
                     else
                         tma_load_3d_mcast(dst + rank * slice_bytes, &tm, fb, x, y + (int)rank * slice_rows, 0, all);
                 }
+                if (++slot == S) { slot = 0; phase ^= 1u; }
             }
             // Every slot this CTA filled is released by its receivers before exit.
             for (int it = total; ok && it < total + S; ++it) {
@@ -127,24 +148,26 @@ tma_bench_kernel(const __grid_constant__ CUtensorMap tm, const BenchParams p) {
     } else if (warp == 1 && lane == 0) {
         uint64_t c0 = 0, g0 = 0;
         uint32_t bad = 0;
-        for (int it = 0; it < total; ++it) {
+        TileWalk tw;
+        tw.init(p, cid, ncl);
+        int slot = 0;
+        uint32_t phase = 0;
+        for (int it = 0; it < total; ++it, tw.next()) {
             if (it == p.warmup) {
                 c0 = clock64();
                 g0 = globaltimer_ns();
             }
-            const int slot = it % S;
-            const uint32_t phase = (uint32_t)(it / S) & 1u;
             if (!bench_wait(smem_u32(&full[slot]), phase, p, 2)) { ok = false; break; }
             // Every 64th load (and the last), check the first and last row of
             // the tile: element (r, j) of a 128-byte-swizzled box sits at
             // r*128 + ((j/8) ^ (r%8))*16 + (j%8)*2. Checking reads global
             // memory, so it stays off most iterations' critical path.
-            int x, y;
-            tile_origin(p, it, cid, ncl, x, y);
+            const bool check = (it & 63) == 0 || it == total - 1;
+            int x = 0, y = 0;
+            if (check) tw.origin(p, x, y);
             const uint8_t* box = smem + slot * box_bytes;
             const int rs[2] = {0, p.box_rows - 1};
             const int js[2] = {0, 63};
-            const bool check = (it & 63) == 0 || it == total - 1;
             for (int a = 0; check && a < 2; ++a) {
                 const int r = rs[a], j = js[a];
                 const uint16_t got = *reinterpret_cast<const uint16_t*>(
@@ -152,14 +175,21 @@ tma_bench_kernel(const __grid_constant__ CUtensorMap tm, const BenchParams p) {
                 const uint16_t want = p.src[(long long)(y + r) * p.ld + x + j];
                 bad += got != want;
             }
+            // Release the slot to every CTA that writes into it: a release where this
+            // thread read the slot, a relaxed arrive where it did not.
             const uint32_t eb = smem_u32(&empty[slot]);
             if (p.mode == TMA_BENCH_UNICAST) {
                 mbar_arrive_local(eb);
             } else if (p.mode == TMA_BENCH_MULTICAST) {
-                mbar_arrive_cluster(mapa(eb, 0));
+                if (check) mbar_arrive_cluster(mapa(eb, 0));
+                else       arrive_relaxed_cluster(mapa(eb, 0));
             } else {
-                for (uint32_t r = 0; r < c; ++r) mbar_arrive_cluster(mapa(eb, r));
+                for (uint32_t r = 0; r < c; ++r) {
+                    if (check) mbar_arrive_cluster(mapa(eb, r));
+                    else       arrive_relaxed_cluster(mapa(eb, r));
+                }
             }
+            if (++slot == S) { slot = 0; phase ^= 1u; }
         }
         p.cycles[blockIdx.x] = clock64() - c0;
         p.ns[blockIdx.x] = globaltimer_ns() - g0;
