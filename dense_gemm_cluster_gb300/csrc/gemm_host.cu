@@ -247,7 +247,6 @@ struct gemm_handle_s {
     unsigned int* flags = nullptr;
     size_t workspace_bytes = 0;
     size_t flag_count = 0;
-    unsigned int epoch = 0;
     bool smem_set[2][2][2] = {};
     int occ_key[2][2][2][9];    // cached max active clusters per (BN, G, BK, cluster size)
 };
@@ -621,15 +620,9 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
             if (e == cudaSuccess) e = cudaMemset(h->flags, 0, slots * sizeof(unsigned int));
             if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "stream-K flags: %s", cudaGetErrorString(e));
             h->flag_count = slots;
-            h->epoch = 0;
-        }
-        if (++h->epoch == 0) {       // flags hold epochs; 0 means "never written"
-            cudaMemsetAsync(h->flags, 0, h->flag_count * sizeof(unsigned int), stream);
-            h->epoch = 1;
         }
         kp.workspace = h->workspace;
         kp.flags = h->flags;
-        kp.epoch = h->epoch;
     }
     void* args[] = {&tmA, &tmB, &tmC, &kp};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
@@ -729,6 +722,8 @@ extern "C" gemm_status_t gemm_query_status(gemm_handle_t h, void* stream_v) {
     fail(&h->err, GEMM_ERR_DEVICE_TIMEOUT, "bounded wait expired: %s (stage/buffer %u, CTA %u, tile %d)", role,
          w[1], w[2], (int)w[3]);
     cudaMemset(h->d_status, 0, 16);
+    // An aborted launch may leave stream-K flags raised; lower them for the next one.
+    if (h->flags) cudaMemset(h->flags, 0, h->flag_count * sizeof(unsigned int));
     return GEMM_ERR_DEVICE_TIMEOUT;
 }
 

@@ -94,8 +94,7 @@ struct KernelParams {
     long long dp_tiles;
     long long sk_iters;
     float* workspace;        // one BLOCK_M x BN fp32 partial slot per CTA of the grid
-    unsigned int* flags;     // per slot: the epoch whose partial the slot holds
-    unsigned int epoch;      // this launch's epoch (never 0)
+    unsigned int* flags;     // per slot: 1 while the slot holds a partial not yet summed, else 0
     int clc;                 // 1: one cluster per tile; running clusters take pending ones' tiles
 };
 
@@ -124,7 +123,10 @@ __device__ __forceinline__ TileCoord tile_coord(const KernelParams& p, long long
 //             the epilogue writes the fp32 partial to this CTA's workspace slot
 //             and raises its flag.
 //   FINISHER: the first part of a tile whose rest other clusters compute; the
-//             epilogue adds their partials (in cluster order) before storing C.
+//             epilogue adds their partials (in cluster order) before storing C,
+//             then lowers their flags, so every launch starts with all flags down
+//             and the kernel carries no per-launch host state (a CUDA graph can
+//             replay it).
 enum : int { WORK_WHOLE = 0, WORK_PARTIAL = 1, WORK_FINISHER = 2 };
 
 struct Work {
@@ -777,7 +779,9 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                        ERR_WAIT_TMEM_FULL, acc, t))
                 dead = true;
             if (dead) {
-                if (w.kind != WORK_WHOLE) epilogue_bar();
+                // the named barriers the live warps reach for this work
+                if (w.kind == WORK_PARTIAL) epilogue_bar();
+                if (w.kind == WORK_FINISHER) { epilogue_bar(); epilogue_bar(); }
                 continue;
             }
             tc_fence_after();
@@ -812,7 +816,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 __threadfence();
                 epilogue_bar();
-                if (warp == 2 && lane == 0) st_release_gpu(&p.flags[slot], p.epoch);
+                if (warp == 2 && lane == 0) st_release_gpu(&p.flags[slot], 1u);
                 continue;
             }
             if (w.kind == WORK_FINISHER) {
@@ -821,7 +825,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (int i = 0; i < w.contrib_count; ++i) {
                         const unsigned int* f = &p.flags[(long long)(w.contrib_first + i) * cs + rank];
                         const uint64_t c0 = clock_cycles();
-                        while (ld_acquire_gpu(f) != p.epoch) {
+                        while (ld_acquire_gpu(f) != 1u) {
                             if (*abort_flag) break;
                             if (clock_cycles() - c0 > 2ull * p.timeout_ns) {
                                 report_timeout(p, ERR_WAIT_PARTIAL, (uint32_t)(w.contrib_first + i), t);
@@ -841,6 +845,14 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             } else {
                 if (w.kind == WORK_FINISHER) store_tile<BN, G, false, true>(p, &tmC, et, stage_ptr, stage_base, buf);
                 else                         store_tile<BN, G, false, false>(p, &tmC, et, stage_ptr, stage_base, buf);
+            }
+            if (w.kind == WORK_FINISHER) {
+                // All four warps have read the partials: lower the contributors' flags
+                // for the next launch (which starts after this one in stream order).
+                epilogue_bar();
+                if (warp == 2 && lane == 0)
+                    for (int i = 0; i < w.contrib_count; ++i)
+                        p.flags[(long long)(w.contrib_first + i) * cs + rank] = 0u;
             }
         }
         if (lane == 0) bulk_wait_group<0>();

@@ -177,3 +177,34 @@ def test_sub_wave_problem_spreads_over_more_clusters(G, M, N, K, opts):
     b = _run(G, p, **opts)
     assert_close(a, p.reference(), K, "f32", f"sub-wave {M}x{N}x{K} {opts}")
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("opts", [dict(schedule="stream_k", max_clusters=5, block_n=256),
+                                  dict(mode="mcast", mcast_b=1, cluster_m=2)])
+def test_gemm_replays_in_a_cuda_graph(G, opts):
+    # A captured gemm_run replays correctly: stream-K partial flags are lowered by the
+    # kernel itself, so no per-launch host state is frozen into the graph. Each replay
+    # recomputes C (beta = 0) into a NaN-filled buffer.
+    import torch
+    from gpu_cases import torch_dev
+    p = Problem(1000, 1100, 448, la="row", lb="col", out="f32", seed=22)
+    g = G.Gemm(0, **options_for(p, **opts))
+    try:
+        dA, dB, dC = torch_dev(p.A), torch_dev(p.B), torch_dev(p.C_in)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):          # first run: workspace, flags, attributes, occupancy
+            g.run(p.M, p.N, p.K, dA, p.lda, dB, p.ldb, dC, p.ldc, 1.0, 0.0, s)
+        s.synchronize()
+        assert g.query_status(s) == G.GEMM_OK
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            g.run(p.M, p.N, p.K, dA, p.lda, dB, p.ldb, dC, p.ldc, 1.0, 0.0, s)
+        ref = p.reference()
+        for rep in range(3):
+            dC.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert_close(p.result(dC), ref, p.K, "f32", f"graph replay {rep} {opts}")
+        assert g.query_status() == G.GEMM_OK
+    finally:
+        g.close()
