@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -561,8 +562,18 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     p.timeout_ns = 2000000000ull;
     void* fn = pair ? reinterpret_cast<void*>(&attention_fwd_kernel<true>)
                     : reinterpret_cast<void*>(&attention_fwd_kernel<false>);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    // Set the shared-memory limit once per device and kernel, so that a steady-state
+    // call is one launch (and can be captured into a CUDA graph).
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));
+    static std::atomic<unsigned char> smem_set[64][2];
+    std::atomic<unsigned char>& flag = smem_set[dev & 63][pair ? 1 : 0];
+    if (!flag.load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));
+        flag.store(1, std::memory_order_release);
+    }
     long long ctas = (sq + QT * TQ - 1) / (QT * TQ);
     ctas = (ctas + cluster - 1) / cluster * cluster;      // whole clusters; extra CTAs store nothing
     cudaLaunchConfig_t cfg;

@@ -132,3 +132,34 @@ def test_attention_more_query_blocks_than_sms():
             base = (o, lse)
         else:
             assert np.array_equal(o, base[0]) and np.array_equal(lse, base[1])
+
+
+@pytest.mark.parametrize("cluster,cta_group", [(2, 1), (2, 2)])
+def test_attention_replays_in_a_cuda_graph(cluster, cta_group):
+    import torch
+    import oracle
+    from dense_gemm_cluster_gb300 import gemm, inputs
+    Q, K, V = _inputs(2, 300, 500, 51)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    dQ, dK, dV = dev(Q), dev(K), dev(V)
+    O = torch.empty(2 * 300 * 128, dtype=torch.float32, device="cuda")
+    lse = torch.empty(2 * 300, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    args = (dQ, dK, dV, O, lse, 2, 300, 500, 128, 0.0, 1, cluster, cta_group)
+    with torch.cuda.stream(s):                      # first call sets the kernel's attributes
+        assert gemm.attention_forward_run(*args, stream=s) == gemm.GEMM_OK
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        assert gemm.attention_forward_run(*args, stream=s) == gemm.GEMM_OK
+    ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True)
+    vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+    for _ in range(3):
+        O.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        o = O.cpu().numpy().reshape(2, 300, 128).astype(np.float64)
+        assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
+        assert np.max(np.abs(lse.cpu().numpy().reshape(2, 300) - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+    assert gemm.attention_forward_query_status() == gemm.GEMM_OK
