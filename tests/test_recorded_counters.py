@@ -1,0 +1,75 @@
+"""The ncu counters recorded under profiles/ against the analytic byte accounting.
+
+`profiles/ncu_traffic.json` holds, per workload, the DRAM bytes and the L2 -> SM
+operand sectors of one launch as ncu measured them on GB300. These tests hold
+those measurements to the design's claims: the pair MMA plus 4-CTA multicast of B
+cuts the measured L2 -> SM operand bytes of the 8192^3 GEMM at least 1.8x against
+unicast tiles, and the measured bytes follow the planner's analytic accounting.
+(No GPU needed: the numbers are read from the committed record.)
+"""
+import json
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def records():
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        return json.load(f)
+
+
+@pytest.fixture(scope="module")
+def analytic():
+    from dense_gemm_cluster_gb300 import build
+    build.build()
+    from dense_gemm_cluster_gb300 import gemm
+    from dense_gemm_cluster_gb300.workloads import WORKLOADS
+    out = {}
+    for name, w in WORKLOADS.items():
+        opts = gemm.make_options(layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out,
+                                 **w.options)
+        s, p = gemm.gemm_plan(opts, w.M, w.N, w.K, w.batch, 152)
+        assert s == 0
+        out[name] = (w, p)
+    return out
+
+
+def test_multicast_and_pair_cut_measured_l2_to_sm_bytes(records, analytic):
+    uni = records["gemm8192_bf16_unicast"]["lts_bytes"]
+    shared = records["gemm8192_bf16_pair_mcastB4"]["lts_bytes"]
+    measured = uni / shared
+    expected = (analytic["gemm8192_bf16_unicast"][1].l2_to_sm_operand_bytes /
+                analytic["gemm8192_bf16_pair_mcastB4"][1].l2_to_sm_operand_bytes)
+    assert expected == pytest.approx(2.0)
+    assert measured >= 1.8, f"measured L2->SM reduction {measured:.2f}x"
+    assert abs(measured / expected - 1.0) < 0.25
+
+
+@pytest.mark.parametrize("name", ["gemm4096_bf16_cluster2x1", "gemm4096_bf16_cluster2x2", "gemm8192_bf16_pair_mcastB4",
+                                  "gemm8192_bf16_unicast", "scores_8x16x4096x4096x128", "skinny_16384x128x8192",
+                                  "skinny_128x16384x8192"])
+def test_measured_l2_to_sm_bytes_follow_the_analytic_accounting(records, analytic, name):
+    # Measured L2 -> SM reads sit a little below the analytic operand fetches where
+    # requests for the same tile arrive close together (served once), and a little above
+    # where the stream-K partials and beta * C reads come on top of the operands.
+    w, p = analytic[name]
+    ratio = records[name]["lts_bytes"] / p.l2_to_sm_operand_bytes
+    assert 0.75 <= ratio <= 1.3, f"{name}: measured / analytic L2->SM bytes = {ratio:.3f}"
+
+
+@pytest.mark.parametrize("name", ["scores_8x16x4096x4096x128", "skinny_16384x128x8192", "skinny_128x16384x8192",
+                                  "gemm4096_bf16_cluster2x1", "attention_fwd_8x16x4096x4096x128"])
+def test_dram_traffic_of_bandwidth_sensitive_workloads_stays_near_the_algorithmic_bytes(records, analytic, name):
+    # The HBM-bound workloads (and the L2-resident 4096^3 GEMM) read each input from DRAM
+    # about once: no wasted re-reads. (Part of the output may still sit in L2 when the
+    # kernel ends, so the lower bound is loose.)
+    if name.startswith("attention"):
+        from dense_gemm_cluster_gb300.workloads import ATTENTION_WORKLOADS
+        algorithmic = ATTENTION_WORKLOADS[name].min_hbm_bytes()
+    else:
+        algorithmic = analytic[name][0].min_hbm_bytes()
+    ratio = records[name]["dram_bytes"] / algorithmic
+    assert 0.8 <= ratio <= 1.2, f"{name}: DRAM bytes / algorithmic bytes = {ratio:.3f}"
