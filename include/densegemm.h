@@ -86,7 +86,7 @@ typedef struct {
                            multiple of 64 when A or B is K-major (auto picks 64 otherwise) */
     int stages;         /* shared-memory pipeline depth; 0 = as many as fit */
     int max_clusters;   /* cap on the persistent grid, in clusters; 0 = as many as are co-resident */
-    int group_m;        /* raster band height, in cluster tiles along M; 0 = 8 */
+    int group_m;        /* raster band height, in cluster tiles along M; 0 = 4 */
     int schedule;       /* 0 = auto, 1 = whole tiles only, 3 = cluster launch control (one
                            cluster per tile; running clusters cancel pending launches and take
                            their tiles, asking for the next tile before computing the current
