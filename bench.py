@@ -89,6 +89,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+RATED_FLOP_PER_CLK_PER_SM = 8192     # dense bf16 tcgen05 rate of one SM
+RATED_SM_MHZ = 2070                  # GB300 maximum SM clock
+
+
+def rated_tensor_peak(device, clocks) -> dict:
+    """The rated dense-bf16 rate: SMs x 8192 FLOP per clock x the maximum SM clock (the
+    sampled clocks.max.sm when nvidia-smi answered, else 2070 MHz)."""
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz = clocks.get("sm_max_mhz") or RATED_SM_MHZ
+    return {"tflops": sms * RATED_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12, "sms": sms, "sm_mhz": mhz}
+
+
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     for rel in sources:
@@ -384,6 +397,12 @@ def bench_ours(args, w: Workload):
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "peak_source": f"hbm_gbs (copy) of {peaks_kind}",
                     "algorithmic_bytes_per_launch": w.min_hbm_bytes()}
+    clocks = clk.summary()
+    if roofline["bound"] == "tensor":
+        rated = rated_tensor_peak(device, clocks)
+        roofline.update({"rated_peak": rated["tflops"], "frac_of_rated": achieved / rated["tflops"],
+                         "rated_peak_source": f"{rated['sms']} SMs x {RATED_FLOP_PER_CLK_PER_SM} FLOP/clk x "
+                                              f"{rated['sm_mhz']:.0f} MHz"})
     roofline.update({"traffic": traffic_rec["dram_bytes"] if traffic_rec else None,
                      "arithmetic_intensity": intensity, "ridge": ridge,
                      "tflops": w.flops / avg_launch_s / 1e12,
@@ -410,7 +429,7 @@ def bench_ours(args, w: Workload):
                                    "measured": traffic_rec.get("lts_bytes") if traffic_rec else None},
         "gpu_launches": launches,
         "wall_s_timed_region": wall,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
 
     if not args.no_e2e:
@@ -454,7 +473,7 @@ def e2e_through_host_api(g, p: DeviceProblem, args, device, stream, dist):
     h2d = A_h.numel() * 2 + B_h.numel() * 2 + (C_h.numel() * esc if w.beta != 0.0 else 0)
     return {"value": units / elapsed / 1e12, "unit": "TFLOP/s", "steps": steps,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(C_h.numel() * esc),
-            "ms_per_step": 1e3 * elapsed / steps}
+            "ms_per_step": 1e3 * elapsed / steps, "api": "gemm_run_host (C ABI, host buffers)"}
 
 
 # ---------------------------------------------------------------- fused attention workloads
@@ -587,6 +606,8 @@ def bench_attention_ours(args, w: AttentionWorkload):
     avg_launch_s = local_s / args.steps
     achieved = w.flops / avg_launch_s / 1e12
     traffic_rec = recorded_traffic(w.name, ATTN_KERNEL_SOURCES)
+    clocks = clk.summary()
+    rated = rated_tensor_peak(device, clocks)
     line = {
         "metric": ATTN_METRIC, "value": units / elapsed / 1e12, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
@@ -600,13 +621,16 @@ def bench_attention_ours(args, w: AttentionWorkload):
                      "algorithmic_flops_per_launch": w.flops,
                      "traffic": traffic_rec["dram_bytes"] if traffic_rec else None,
                      "arithmetic_intensity": w.flops / w.min_hbm_bytes(),
-                     "ridge": tensor_peak * 1e12 / (hbm_peak * 1e9)},
+                     "ridge": tensor_peak * 1e12 / (hbm_peak * 1e9),
+                     "rated_peak": rated["tflops"], "frac_of_rated": achieved / rated["tflops"],
+                     "rated_peak_source": f"{rated['sms']} SMs x {RATED_FLOP_PER_CLK_PER_SM} FLOP/clk x "
+                                          f"{rated['sm_mhz']:.0f} MHz"},
         "gpu_launches": launches - launches0,
         "wall_s_timed_region": wall,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if not args.no_e2e:
-        line["e2e"] = attn_e2e(w, args, device, stream, dist, run, (Qh, Kh, Vh), (Q, K, V), (O, lse))
+        line["e2e"] = attn_e2e(w, args, device, stream, dist, cluster, cta_group, (Qh, Kh, Vh))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         _, rate, secs, heads, threads = attn_oracle_sample(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -618,23 +642,26 @@ def bench_attention_ours(args, w: AttentionWorkload):
     return 0
 
 
-def attn_e2e(w, args, device, stream, dist, run, host_in, dev_in, dev_out):
-    """The same metric with Q, K, V copied in from pinned host memory and O, lse copied out every step."""
+def attn_e2e(w, args, device, stream, dist, cluster, cta_group, host_in):
+    """The same metric through attention_forward_run_host: Q, K, V in from pinned host
+    memory and O, lse back, every step (the call pipelines the copies over parts of the heads)."""
     import numpy as np
     import torch
-    pinned = [torch.from_numpy(a.reshape(-1).view(np.int16)).pin_memory() for a in host_in]
-    O, lse = dev_out
-    O_h = torch.empty(O.numel(), dtype=O.dtype).pin_memory()
-    lse_h = torch.empty(lse.numel(), dtype=lse.dtype).pin_memory()
+    from dense_gemm_cluster_gb300 import gemm
+    Qp, Kp, Vp = [torch.from_numpy(a.reshape(-1).view(np.int16)).pin_memory() for a in host_in]
+    odt = torch.float32 if w.out == "f32" else torch.int16
+    out_f32 = 1 if w.out == "f32" else 0
+    O_h = torch.empty(w.batch * w.sq * w.d, dtype=odt).pin_memory()
+    lse_h = torch.empty(w.batch * w.sq, dtype=torch.float32).pin_memory()
+    ws_bytes = gemm.attention_forward_host_workspace_bytes(w.batch, w.sq, w.sk, w.d, out_f32)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     steps = max(1, min(args.steps, args.e2e_steps))
 
     def step():
-        for d_, h_ in zip(dev_in, pinned):
-            d_.copy_(h_, non_blocking=True)
-        run()
-        O_h.copy_(O, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        stream.synchronize()
+        s = gemm.attention_forward_run_host(Qp, Kp, Vp, O_h, lse_h, w.batch, w.sq, w.sk, w.d, ws, ws_bytes, 0.0,
+                                            out_f32, cluster, cta_group, stream)
+        if s != gemm.GEMM_OK:
+            raise RuntimeError(f"attention_forward_run_host: status {s}")
 
     for _ in range(2):
         step()
@@ -644,10 +671,12 @@ def attn_e2e(w, args, device, stream, dist, run, host_in, dev_in, dev_out):
         step()
     local = time.perf_counter() - t0
     elapsed, units = aggregate(dist, local, float(w.flops) * steps, device)
-    h2d = sum(int(h_.numel()) * 2 for h_ in pinned)
+    h2d = int((Qp.numel() + Kp.numel() + Vp.numel()) * 2)
     d2h = int(O_h.numel() * O_h.element_size() + lse_h.numel() * 4)
+    del ws
     return {"value": units / elapsed / 1e12, "unit": "TFLOP/s", "steps": steps, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * elapsed / steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * elapsed / steps,
+            "api": "attention_forward_run_host (C ABI, host buffers)"}
 
 
 def main(argv=None):

@@ -43,7 +43,7 @@ class gemm_options_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "mode", "mcast_a", "mcast_b", "cluster_m", "cluster_n", "cta_group", "layout_a", "layout_b",
         "layout_c", "out_type", "block_n", "block_k", "stages", "max_clusters", "group_m", "schedule")] + [
-        ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_int)]
+        ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_int), ("host_parts", ctypes.c_int)]
 
 
 class gemm_plan_t(ctypes.Structure):
@@ -307,3 +307,22 @@ def attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, scale=0.0, out_f32=
 
 def attention_forward_query_status(stream=None) -> int:
     return _lib.attention_forward_query_status(_stream(stream))
+
+
+_lib.attention_forward_run_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _i32,
+                                            _i32, _vp, ctypes.c_size_t, _vp]
+_lib.attention_forward_run_host.restype = _i32
+_lib.attention_forward_host_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i32]
+_lib.attention_forward_host_workspace_bytes.restype = ctypes.c_size_t
+
+
+def attention_forward_host_workspace_bytes(batch, sq, sk, d, out_f32=0) -> int:
+    return _lib.attention_forward_host_workspace_bytes(batch, sq, sk, d, out_f32)
+
+
+def attention_forward_run_host(Q, K, V, O, lse, batch, sq, sk, d, workspace, workspace_bytes, scale=0.0, out_f32=0,
+                               cluster=1, cta_group=1, stream=None) -> int:
+    """Host Q, K, V, O, lse (numpy arrays or pinned CPU tensors); `workspace` is device memory."""
+    return _lib.attention_forward_run_host(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), batch, sq, sk, d, scale,
+                                           out_f32, cluster, cta_group, _ptr(workspace), workspace_bytes,
+                                           _stream(stream))

@@ -93,13 +93,22 @@ typedef struct {
                            one), 2 = stream-K tail: the tiles
                            left after the last full wave (between one and two waves'
                            worth) are split by k-blocks evenly over all clusters, and the
-                           parts are summed in a fixed order. Auto uses it when whole tiles
-                           would leave the last wave under 90 % full. Needs a handle-owned
+                           parts are summed in a fixed order; with fewer tiles than
+                           clusters, the k-blocks are spread over more clusters (at least
+                           16 k-blocks each). Auto splits the tail when that saves at least
+                           4 us of an estimated tile time (the tile's FLOPs at 1.5 PFLOP/s
+                           shared by all SMs), and spreads a problem with fewer tiles than
+                           clusters only when at most half of the clusters would have one.
+                           Needs a handle-owned
                            workspace (one 128 x block_n fp32 tile per CTA), so
                            gemm_run_noalloc always runs whole tiles. */
     uint64_t wait_timeout_ns; /* bound on every in-kernel wait, counted as 2 SM cycles per ns
                                  (this long at 2 GHz, longer at lower clocks); 0 = 2 s */
     int debug_flags;    /* 0, or GEMM_DEBUG_EXTRA_TX (tests only) */
+    int host_parts;     /* gemm_run_host: parts the problem is split into for overlapping the
+                           host copies with the GEMMs, 1 to 8 (fewer when the split dimension
+                           is short: parts are multiples of 256 lines); 0 = the count a model
+                           of the copy and GEMM times picks */
 } gemm_options_t;
 
 /* What gemm_run would launch for a given problem (host arithmetic only). */
@@ -157,7 +166,15 @@ gemm_status_t gemm_run_strided_batched(gemm_handle_t h, int64_t M, int64_t N, in
 
 /* gemm_run on HOST buffers: copies A, B (and C when beta != 0) to device staging
  * owned by the handle, runs, copies C back, and synchronizes `stream` before
- * returning. Host buffers may be pageable or pinned; pinned copies are faster. */
+ * returning. The problem is split along the larger of M and N into parts
+ * (options.host_parts, or a count a model of the copy and GEMM times picks): the
+ * operand every part needs is copied in whole, then part i's slice of the other
+ * operand (and of C) is copied in on a handle-owned stream while part i-1 runs
+ * on `stream` and part i-2's C is copied out on another, so the copies in both
+ * directions overlap each other and the GEMMs. Only the elements of each line
+ * are copied (pitched copies): the padding of a leading dimension is neither
+ * read nor written on the host. Host buffers may be pageable or pinned; pinned
+ * copies are faster and only they overlap. */
 gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                             const void *A, int64_t lda, const void *B, int64_t ldb,
                             void *C, int64_t ldc, float alpha, float beta, void *stream);

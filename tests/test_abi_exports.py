@@ -98,6 +98,8 @@ def test_plan_column_major_c_swaps_roles(lib):
     (dict(layout_a=2), 1),
     (dict(out_type=7), 1),
     (dict(mode=5), 1),
+    (dict(host_parts=9), 1),
+    (dict(host_parts=-1), 1),
 ])
 def test_plan_rejects_bad_options(lib, kw, code):
     s, _ = plan(lib, 128, 128, 128, **kw)
@@ -159,6 +161,11 @@ def test_plan_sub_wave_spread(lib):
     assert p.tiles == 128 and p.clusters == 128 and p.stream_k_tiles == 0
     s, p = plan(lib, 768, 128, 8192, sm=152, block_n=128, schedule="dp")
     assert p.clusters == 6 and p.stream_k_tiles == 0
+    # an explicit stream-K schedule spreads even when more than half the clusters are busy
+    s, p = plan(lib, 16384, 128, 8192, sm=152, block_n=128, schedule="stream_k")
+    assert p.tiles == 128 and p.clusters == 152 and p.stream_k_tiles == 128
+    s, p = plan(lib, 16384, 128, 8192, sm=152, block_n=128, cta_group=2, cluster_m=2, schedule="stream_k")
+    assert p.tiles == 64 and p.clusters == 76 and p.stream_k_tiles == 64
     s, p = plan(lib, 256, 256, 256, sm=152, mode="mcast", mcast_b=1, cluster_m=2)
     assert p.tiles == 1 and p.clusters == 1
 
@@ -180,3 +187,14 @@ def test_attention_validation_before_launch(lib):
     assert run(a, a, a, a, None, 1 << 16, 128, 128, 128) == lib.GEMM_ERR_INVALID_ARG      # batch limit
     assert run(a, a, a, a, None, 0, 128, 128, 128) == lib.GEMM_OK                         # nothing to do
     assert run(a, a, a, a, None, 3, 0, 128, 128) == lib.GEMM_OK
+    # the host-buffer entry point checks its workspace and arguments before any copy
+    need = lib.attention_forward_host_workspace_bytes(2, 300, 500, 128, 0)
+    assert need >= 2 * (300 + 2 * 500) * 128 * 2 + 2 * 300 * (128 * 2 + 4)
+    assert lib.attention_forward_host_workspace_bytes(0, 300, 500, 128, 0) == 0
+    host = lib.attention_forward_run_host
+    assert host(a, a, a, a, None, 2, 300, 500, 128, a, need - 1) == lib.GEMM_ERR_INVALID_ARG     # short
+    assert host(a, a, a, a, None, 2, 300, 500, 128, None, need) == lib.GEMM_ERR_INVALID_ARG      # missing
+    assert host(a, a, a, a, None, 2, 300, 500, 128, a + 16, need) == lib.GEMM_ERR_ALIGNMENT     # not 256-B aligned
+    assert host(a, a, a, a, None, 2, 300, 500, 64, a, need) == lib.GEMM_ERR_UNSUPPORTED
+    assert host(a, a, a, a, None, 2, 300, 500, 128, a, need, cluster=4, cta_group=2) == lib.GEMM_ERR_UNSUPPORTED
+    assert host(a, a, a, a, None, 0, 300, 500, 128, None, 0) == lib.GEMM_OK                     # nothing to do

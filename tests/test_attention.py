@@ -163,3 +163,29 @@ def test_attention_replays_in_a_cuda_graph(cluster, cta_group):
         assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
         assert np.max(np.abs(lse.cpu().numpy().reshape(2, 300) - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
     assert gemm.attention_forward_query_status() == gemm.GEMM_OK
+
+
+@pytest.mark.parametrize("b,sq,sk,cluster,cta_group,with_lse", [
+    (10, 300, 500, 2, 1, True),       # 5 parts of 2 heads
+    (11, 301, 257, 1, 1, True),       # sq odd: parts of 4 heads keep each lse view 16-byte aligned
+    (9, 258, 130, 2, 2, False),       # sq even, not a multiple of 4: parts of 2 heads; no lse
+    (1, 128, 128, 4, 1, True),        # a single part
+])
+def test_attention_host_entry_equals_device_entry(b, sq, sk, cluster, cta_group, with_lse):
+    # attention_forward_run_host copies host Q, K, V into the workspace part by part and
+    # runs the same kernel on each part, so it must equal the device entry bit for bit.
+    import torch
+    from dense_gemm_cluster_gb300 import gemm
+    Q, K, V = _inputs(b, sq, sk, 300 + sq)
+    ref_o, ref_lse = _run(Q, K, V, cluster, out_f32=1, cta_group=cta_group)
+    O_h = np.full(b * sq * 128, np.nan, dtype=np.float32)
+    lse_h = np.full(b * sq, np.nan, dtype=np.float32) if with_lse else None
+    ws_bytes = gemm.attention_forward_host_workspace_bytes(b, sq, sk, 128, 1)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    host = lambda a: np.ascontiguousarray(a).view(np.int16)
+    s = gemm.attention_forward_run_host(host(Q), host(K), host(V), O_h, lse_h, b, sq, sk, 128, ws, ws_bytes, 0.0, 1,
+                                        cluster, cta_group)
+    assert s == gemm.GEMM_OK
+    assert np.array_equal(O_h.reshape(b, sq, 128).astype(np.float64), ref_o)
+    if with_lse:
+        assert np.array_equal(lse_h.reshape(b, sq).astype(np.float64), ref_lse)

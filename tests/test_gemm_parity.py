@@ -145,6 +145,7 @@ def test_128_wide_stages_single_cta_tiles(G, cm, cn, ma, mb, la, lb):
     (520, 384, 1024, 7, 128, "f32", 0.5),       # ragged tiles, beta read once by each finisher
     (256, 256, 2048, 3, 256, "bf16", 1.0),      # 2 tiles over 3 clusters: every tile split
     (129, 1000, 960, 6, 128, "f32", 0.0),       # many contributors per tile
+    (1024, 128, 4096, 12, 128, "bf16", 0.0),    # 8 tiles spread over 12 clusters (more than half busy)
 ])
 def test_stream_k_tail_matches_oracle(G, M, N, K, max_clusters, bn, out, beta):
     p = Problem(M, N, K, la="row", lb="col", out=out, beta=beta, seed=9)

@@ -96,6 +96,13 @@ def test_pair_stream_k_tail(G, cm, cn, ma, mb):
     assert_close(got, p.reference(1.0, 0.5), 1152, "bf16", f"pair stream-K {cm}x{cn}")
 
 
+def test_pair_stream_k_spreads_when_most_pairs_are_busy(G):
+    # 4 pair tiles on 6 pairs: an explicit stream-K schedule splits every tile's k-blocks
+    p = Problem(1024, 256, 4096, la="row", lb="row", out="f32", seed=20)
+    got = _run(G, p, cta_group=2, cluster_m=2, schedule="stream_k", max_clusters=6)
+    assert_close(got, p.reference(), 4096, "f32", "pair stream-K spread")
+
+
 def test_pair_sub_wave_problem_spreads_over_more_clusters(G):
     # 2 pair tiles of 256x256 with 64 k-blocks each: the auto schedule splits them over more pairs
     p = Problem(512, 256, 8192, la="row", lb="col", out="bf16", beta=0.5, seed=19)
