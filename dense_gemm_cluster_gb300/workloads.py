@@ -77,8 +77,9 @@ WORKLOADS = {
                     "N(0,1) bf16 Q/K, fp32 S, each K tile multicast across the 4 Q-tile CTAs of a cluster"),
     "skinny_16384x128x8192": Workload(
         "skinny_16384x128x8192", 16384, 128, 8192, dist="uniform",
-        options=dict(mode="mcast", mcast_b=1, cluster_m=4, cluster_n=1, block_n=128),
-        description="skinny GEMM M=16384, N=128, K=8192, U(-1,1), bf16 out, small B multicast along M"),
+        options=dict(mode="mcast", mcast_b=1, cluster_m=4, cluster_n=1, cta_group=2, block_n=128),
+        description="skinny GEMM M=16384, N=128, K=8192, U(-1,1), bf16 out, cta_group::2 256x128 tiles, small B "
+                    "multicast along M across the two pairs of a 4-CTA cluster"),
     "skinny_128x16384x8192": Workload(
         "skinny_128x16384x8192", 128, 16384, 8192, dist="uniform",
         options=dict(mode="mcast", mcast_a=1, cluster_m=1, cluster_n=4, block_n=128),
