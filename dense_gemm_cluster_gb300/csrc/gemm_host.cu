@@ -105,9 +105,10 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
 
     const int BN = o.block_n ? o.block_n : 256;
     // 1024 for aligning the dynamic base, the epilogue staging, then per stage a
-    // full and an empty barrier, plus 5 barriers, the TMEM address, the abort flag
-    // and the epilogue warps' agreement words.
-    const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 5 * 8 + 32 + 256;   // + the tile-id ring
+    // full and an empty barrier, plus 9 barriers (accumulators, drain, and one per
+    // epilogue warp for staging stream-K partials), the TMEM address, the abort
+    // flag and the epilogue warps' agreement words.
+    const int fixed = 1024 + dgc::EPI_SMEM_BYTES + 9 * 8 + 32 + 256;   // + the tile-id ring
     auto stage_bytes_for = [&](int bk) { return dgc::BLOCK_M * bk * 2 + (BN / G) * bk * 2; };
     // Operands as launched (after the C^T transpose): K-major ones need K % 64 == 0
     // for the k-split map that 128-wide stages use.
@@ -888,8 +889,12 @@ extern "C" gemm_status_t gemm_query_status(gemm_handle_t h, void* stream_v) {
     if (w[0] == 0) return GEMM_OK;
     static const char* roles[] = {"none", "producer waiting for a free stage", "MMA waiting for stage bytes",
                                   "MMA waiting for a free accumulator", "epilogue waiting for an accumulator",
-                                  "teardown waiting for in-flight MMAs"};
-    const char* role = w[0] < 6 ? roles[w[0]] : "unknown";
+                                  "teardown waiting for in-flight MMAs",
+                                  "stream-K finisher waiting for another cluster's partial",
+                                  "a role waiting for a tile id from cluster launch control",
+                                  "the scheduler waiting for a free tile-id slot",
+                                  "stream-K finisher waiting for partials copied into shared memory"};
+    const char* role = w[0] < 10 ? roles[w[0]] : "unknown";
     fail(&h->err, GEMM_ERR_DEVICE_TIMEOUT, "bounded wait expired: %s (stage/buffer %u, CTA %u, tile %d)", role,
          w[1], w[2], (int)w[3]);
     cudaMemset(h->d_status, 0, 16);

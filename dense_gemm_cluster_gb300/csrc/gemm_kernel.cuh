@@ -66,6 +66,7 @@ enum : uint32_t {
     ERR_WAIT_PARTIAL = 6,    // stream-K finisher waiting for another cluster's partial
     ERR_WAIT_TILE_ID = 7,    // a role waiting for the next tile from cluster launch control
     ERR_WAIT_TILE_SLOT = 8,  // the scheduler waiting for a free tile-id slot
+    ERR_WAIT_FIXUP = 9,      // stream-K finisher waiting for partials copied into shared memory
 };
 
 constexpr int TILE_RING = 4;   // cluster-launch-control responses in flight per cluster
@@ -435,6 +436,24 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     return true;
 }
 
+// Where a stream-K finisher's epilogue warp stages the partials it adds: its
+// quarter of the operand ring, free once the finisher's last MMA has completed
+// (the finisher is always a cluster's last work item, so no load lands there
+// any more), filled by bulk copies that complete on the warp's own barrier.
+struct FixStage {
+    uint8_t* ptr;        // generic address of the warp's region
+    uint32_t saddr;      // its shared-memory address
+    uint32_t bytes;      // region size
+    uint32_t bar;        // the warp's barrier
+    uint32_t* phase;     // its next phase
+    volatile int* abort_flag;
+};
+
+__device__ __forceinline__ void bulk_load_smem(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 // One epilogue warp's rows of one output tile.
 struct EpiTile {
     uint32_t t_row;      // TMEM address of this warp's lanes, this accumulator's column 0
@@ -451,40 +470,84 @@ struct EpiTile {
 // TMEM -> registers -> (stream-K partials) -> alpha * acc + beta * C_in -> bf16/fp32
 // -> 128-byte-swizzled shared rows -> TMA store, in 128-byte-wide column chunks,
 // double-buffered per warp. Specialised on the output type and on whether
-// partials are added, so whole tiles run the lean loop.
+// partials are added, so whole tiles run the lean loop. Returns false when a
+// wait ran out (the CTA is aborting).
+//
+// Partial slots hold [row quarter][column / 4][32 rows][4] floats, so one warp's
+// share of a run of columns is contiguous: a finisher copies each contributor's
+// share of as many chunks as fit in its staging region in one bulk copy, and
+// reads it back conflict-free (lanes on consecutive 16-byte words).
 template <int BN, int G, bool OUT_F32, bool FIXUP>
-__device__ __forceinline__ void store_tile(const KernelParams& p, const CUtensorMap* tmC, const EpiTile& e,
-                                           uint8_t* stage_ptr, uint32_t stage_base, uint32_t& buf) {
+__device__ __forceinline__ bool store_tile(const KernelParams& p, const CUtensorMap* tmC, const EpiTile& e,
+                                           uint8_t* stage_ptr, uint32_t stage_base, uint32_t& buf,
+                                           const FixStage& fs) {
     constexpr int CW = OUT_F32 ? 32 : 64;             // columns per 128-byte store row
     constexpr int chunks = BN / CW;
+    constexpr uint32_t CHUNK_BYTES = (CW / 4) * 512;  // one contributor's chunk for one warp
     const bool use_beta = p.beta != 0.0f;
+    const int q = e.trow >> 5;
+    // Chunks per staged pass (0: the partials do not fit, add them from global memory).
+    const int per_pass = FIXUP && e.contrib_count > 0
+                             ? (int)(fs.bytes / (CHUNK_BYTES * (uint32_t)e.contrib_count)) : 0;
+    int pass_c0 = 0, pass_n = 0;
     for (int c = 0; c < chunks; ++c) {
         const int col0 = e.n0 + c * CW;
+        if (FIXUP && per_pass > 0 && c == pass_c0 + pass_n) {
+            // Stage the next pass: every contributor's share of chunks [c, c + pass_n).
+            pass_c0 = c;
+            pass_n = min(per_pass, chunks - c);
+            const uint32_t bytes = (uint32_t)pass_n * CHUNK_BYTES;
+            fence_proxy_async_smem();                      // this lane's reads of the previous pass
+            __syncwarp();                                  // ... by every lane, before it is overwritten
+            if (e.lane == 0) {
+                mbar_arrive_expect_tx_local(fs.bar, bytes * (uint32_t)e.contrib_count);
+                for (int i = 0; i < e.contrib_count; ++i) {
+                    const float4* src =
+                        reinterpret_cast<const float4*>(
+                            p.workspace +
+                            ((long long)(e.contrib_first + i) * e.cs + e.rank) * (long long)(BLOCK_M * BN)) +
+                        ((long long)q * (BN / 4) + (long long)c * (CW / 4)) * 32;
+                    bulk_load_smem(fs.saddr + (uint32_t)i * bytes, src, bytes, fs.bar);
+                }
+            }
+            if (!wait_bounded(fs.bar, *fs.phase, p, fs.abort_flag, ERR_WAIT_FIXUP, (uint32_t)c, -1)) return false;
+            *fs.phase ^= 1u;
+        }
         float v[CW];
         {
             uint32_t r[32];
             tmem_ld_32cols(e.t_row + c * CW, r);
-            tmem_ld_wait();
+            if (!OUT_F32) {
+                uint32_t r2[32];
+                tmem_ld_32cols(e.t_row + c * CW + 32, r2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[(CW - 32) + i] = __uint_as_float(r2[i]);
+            } else {
+                tmem_ld_wait();
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         }
-        if (!OUT_F32) {
-            uint32_t r[32];
-            tmem_ld_32cols(e.t_row + c * CW + 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[(CW - 32) + i] = __uint_as_float(r[i]);
-        }
         if (FIXUP) {
-            // Add the other contributors' partials, in cluster order ([column / 4][row][4] slots).
+            // Add the other contributors' partials, in cluster order.
             for (int i = 0; i < e.contrib_count; ++i) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(
-                        p.workspace + ((long long)(e.contrib_first + i) * e.cs + e.rank) * (long long)(BLOCK_M * BN)) +
-                    (long long)(c * (CW / 4)) * BLOCK_M + e.trow;
+                const float4* src;
+                int stride;
+                if (per_pass > 0) {
+                    src = reinterpret_cast<const float4*>(
+                              fs.ptr + ((size_t)i * pass_n + (size_t)(c - pass_c0)) * CHUNK_BYTES) + e.lane;
+                    stride = 32;
+                } else {
+                    src = reinterpret_cast<const float4*>(
+                              p.workspace +
+                              ((long long)(e.contrib_first + i) * e.cs + e.rank) * (long long)(BLOCK_M * BN)) +
+                          ((long long)q * (BN / 4) + (long long)c * (CW / 4)) * 32 + e.lane;
+                    stride = 32;
+                }
 #pragma unroll
                 for (int j = 0; j < CW / 4; ++j) {
-                    const float4 a = src[j * BLOCK_M];
+                    const float4 a = src[j * stride];
                     v[4 * j] += a.x;
                     v[4 * j + 1] += a.y;
                     v[4 * j + 2] += a.z;
@@ -570,6 +633,7 @@ __device__ __forceinline__ void store_tile(const KernelParams& p, const CUtensor
         }
         buf ^= 1u;
     }
+    return true;
 }
 
 template <int BN, int G, int BK>
@@ -596,7 +660,8 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t* tfull_bar = bars + 2 * S;
     uint64_t* tempty_bar = bars + 2 * S + 2;
     uint64_t* drain_bar = bars + 2 * S + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    uint64_t* fix_bar = bars + 2 * S + 5;               // one per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 9);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     uint8_t* ring = reinterpret_cast<uint8_t*>(((reinterpret_cast<uintptr_t>(tmem_slot + 6)) + 15) & ~uintptr_t(15));
     const uint32_t ring_resp0 = smem_u32(ring);                                // TILE_RING x 16 bytes
@@ -629,6 +694,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(smem_u32(&tempty_bar[i]), (uint32_t)(G * EPI_WARPS));
         }
         mbar_init(smem_u32(drain_bar), 1);
+        for (int i = 0; i < EPI_WARPS; ++i) mbar_init(smem_u32(&fix_bar[i]), 1);
         for (int i = 0; i < TILE_RING; ++i) {
             mbar_init(smem_u32(&ring_full[i]), 1);
             // every CTA's two producers, MMA thread and four epilogue warps read each response
@@ -763,6 +829,11 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t tempty_addr = (G == 2) ? mapa(smem_u32(&tempty_bar[0]), leader) : smem_u32(&tempty_bar[0]);
         ClcCtx epi_clc = clc_ctx;
         epi_clc.arrive = lane == 0;
+        uint32_t fix_phase = 0;
+        const uint32_t ring_bytes = (uint32_t)S * (A_BYTES + B_BYTES);
+        const uint32_t region = (ring_bytes / EPI_WARPS) & ~511u;
+        const FixStage fs{sA + ew * region, smem_u32(sA) + (uint32_t)ew * region, region, smem_u32(&fix_bar[ew]),
+                          &fix_phase, abort_flag};
         WorkIter wi;
         wi.init(p, cluster, clusters, &epi_clc);
         Work w;
@@ -793,9 +864,11 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             if (w.kind == WORK_PARTIAL) {
                 // Part of a tile another cluster finishes: park the fp32 partial. A slot
-                // holds [column / 4][row][4] floats, so the 32 rows of a warp write 512
-                // contiguous bytes per store.
-                float4* dst = reinterpret_cast<float4*>(p.workspace + slot * (long long)(BLOCK_M * BN)) + trow;
+                // holds [row quarter][column / 4][32 rows][4] floats: the 32 rows of a
+                // warp write 512 contiguous bytes per store, and the warp's share of the
+                // slot is contiguous for the finisher's bulk copies.
+                float4* dst = reinterpret_cast<float4*>(p.workspace + slot * (long long)(BLOCK_M * BN)) +
+                              (long long)q * (BN / 4) * 32 + lane;
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32cols(t_row + c * 32, r);
@@ -810,7 +883,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        dst[(c * 8 + j) * BLOCK_M] =
+                        dst[(c * 8 + j) * 32] =
                             make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                 }
@@ -839,13 +912,15 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             const EpiTile et{t_row, n0, m0 + q * 32, row, trow, tc.b, lane, tempty_addr + 8u * acc,
                              w.contrib_first, w.contrib_count, cs, (int)rank};
+            bool stored;
             if (p.out_f32) {
-                if (w.kind == WORK_FINISHER) store_tile<BN, G, true, true>(p, &tmC, et, stage_ptr, stage_base, buf);
-                else                         store_tile<BN, G, true, false>(p, &tmC, et, stage_ptr, stage_base, buf);
+                if (w.kind == WORK_FINISHER) stored = store_tile<BN, G, true, true>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
+                else                         stored = store_tile<BN, G, true, false>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
             } else {
-                if (w.kind == WORK_FINISHER) store_tile<BN, G, false, true>(p, &tmC, et, stage_ptr, stage_base, buf);
-                else                         store_tile<BN, G, false, false>(p, &tmC, et, stage_ptr, stage_base, buf);
+                if (w.kind == WORK_FINISHER) stored = store_tile<BN, G, false, true>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
+                else                         stored = store_tile<BN, G, false, false>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
             }
+            if (!stored) dead = true;
             if (w.kind == WORK_FINISHER) {
                 // All four warps have read the partials: lower the contributors' flags
                 // for the next launch (which starts after this one in stream order).

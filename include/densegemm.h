@@ -53,7 +53,7 @@ typedef struct gemm_handle_s *gemm_handle_t;
 typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = 1,    /* a null handle/pointer, negative size, ld too small, bad enum */
-    GEMM_ERR_UNSUPPORTED = 2,    /* a mode / cluster / cta_group combination this build does not run */
+    GEMM_ERR_UNSUPPORTED = 2,    /* a mode / cluster / cta_group combination the library does not run */
     GEMM_ERR_ALIGNMENT = 3,      /* a base pointer not 16-byte aligned, or ld/stride bytes not a multiple of 16 */
     GEMM_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed; see gemm_last_error() */
     GEMM_ERR_DEVICE_TIMEOUT = 5, /* a bounded in-kernel wait expired; the kernel stopped cleanly */
