@@ -477,9 +477,12 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
                         "A and B must be 16-byte aligned with lda*2 and ldb*2 multiples of 16");
         if (batch > 1 && ((strideA * 2) % 16 || (strideB * 2) % 16 || strideA < 0 || strideB < 0))
             return fail(&h->err, GEMM_ERR_ALIGNMENT, "strideA*2 and strideB*2 must be non-negative multiples of 16");
+        // A stride of 0 shares one matrix across the batch; any other stride must keep the
+        // matrices apart (a tensor map cannot describe overlapping ones).
+        if (batch > 1 && ((strideA != 0 && strideA < lda * a_outer) || (strideB != 0 && strideB < ldb * b_outer)))
+            return fail(&h->err, GEMM_ERR_INVALID_ARG,
+                        "strideA and strideB must be 0 (one matrix for every product) or keep the matrices apart");
     }
-    (void)a_outer;
-    (void)b_outer;
 
     int prev = 0;
     cudaGetDevice(&prev);
@@ -520,27 +523,30 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     const int BK = pl.block_k;
     const int atoms = BK / dgc::ATOM_K;
     const bool kmap4 = (r.K % dgc::ATOM_K) == 0;
+    // An operand shared by every product is mapped as a single matrix.
+    const bool a_shared = batch > 1 && opA.stride == 0, b_shared = batch > 1 && opB.stride == 0;
+    const int64_t batch_a = a_shared ? 1 : batch, batch_b = b_shared ? 1 : batch;
     CUtensorMap tmA, tmB, tmC;
     uint32_t br, ba;
     if (!opA.mn_major && kmap4) {
         ksplit_box(dgc::BLOCK_M, atoms, gA, br, ba);
-        s = encode_ksplit(h, &tmA, opA.ptr, r.K, r.M, batch, opA.ld, opA.stride, br, ba, "A");
+        s = encode_ksplit(h, &tmA, opA.ptr, r.K, r.M, batch_a, opA.ld, opA.stride, br, ba, "A");
     } else if (!opA.mn_major) {
-        s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.K, r.M, batch, opA.ld, opA.stride,
+        s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.K, r.M, batch_a, opA.ld, opA.stride,
                        64, dgc::BLOCK_M / gA, "A");
     } else {
-        s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.M, r.K, batch, opA.ld, opA.stride,
+        s = encode_map(h, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opA.ptr, r.M, r.K, batch_a, opA.ld, opA.stride,
                        64, BK / gA, "A");
     }
     if (s != GEMM_OK) return s;
     if (!opB.mn_major && kmap4) {
         ksplit_box(BN / G, atoms, gB, br, ba);
-        s = encode_ksplit(h, &tmB, opB.ptr, r.K, r.N, batch, opB.ld, opB.stride, br, ba, "B");
+        s = encode_ksplit(h, &tmB, opB.ptr, r.K, r.N, batch_b, opB.ld, opB.stride, br, ba, "B");
     } else if (!opB.mn_major) {
-        s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.K, r.N, batch, opB.ld, opB.stride,
+        s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.K, r.N, batch_b, opB.ld, opB.stride,
                        64, (BN / G) / gB, "B");
     } else {
-        s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.N, r.K, batch, opB.ld, opB.stride,
+        s = encode_map(h, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, opB.ptr, r.N, r.K, batch_b, opB.ld, opB.stride,
                        64, BK / gB, "B");
     }
     if (s != GEMM_OK) return s;
@@ -557,6 +563,8 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     kp.num_kb = (int)ceil_div(r.K, BK);
     kp.a_kmap4 = !opA.mn_major && kmap4;
     kp.b_kmap4 = !opB.mn_major && kmap4;
+    kp.a_shared = a_shared ? 1 : 0;
+    kp.b_shared = b_shared ? 1 : 0;
     kp.cx = pl.cluster_m;
     kp.cy = pl.cluster_n;
     kp.mcast_a = r.mcast_a;
@@ -863,6 +871,114 @@ extern "C" gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, in
     }
     // Whatever happened, nothing may still read or write the caller's host
     // buffers once this returns.
+    const cudaError_t e_in = cudaStreamSynchronize(h->pipe_in);
+    const cudaError_t e_out = cudaStreamSynchronize(h->pipe_out);
+    const cudaError_t e_s = cudaStreamSynchronize(stream);
+    if (s != GEMM_OK) return s;
+    if (e == cudaSuccess) e = e_in != cudaSuccess ? e_in : (e_out != cudaSuccess ? e_out : e_s);
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "host copy pipeline: %s", cudaGetErrorString(e));
+    return GEMM_OK;
+}
+
+// gemm_run_strided_batched on host buffers: the batch is split into parts of
+// whole products, pipelined like gemm_run_host's parts. An operand with stride 0
+// (one matrix for every product) is copied once, first.
+extern "C" gemm_status_t gemm_run_strided_batched_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                                       const void* A, int64_t lda, int64_t strideA, const void* B,
+                                                       int64_t ldb, int64_t strideB, void* C, int64_t ldc,
+                                                       int64_t strideC, int64_t batch, float alpha, float beta,
+                                                       void* stream_v) {
+    if (!h) return fail(nullptr, GEMM_ERR_INVALID_ARG, "null handle");
+    if (M < 0 || N < 0 || K < 0 || batch < 0) return fail(&h->err, GEMM_ERR_INVALID_ARG, "negative size");
+    if (M == 0 || N == 0 || batch == 0) return GEMM_OK;
+    if (batch == 1) return gemm_run_host(h, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream_v);
+    const gemm_options_t& o = h->opt;
+    const int esc = o.out_type == GEMM_OUT_F32 ? 4 : 2;
+    if (!C || (K > 0 && (!A || !B))) return fail(&h->err, GEMM_ERR_INVALID_ARG, "null host pointer");
+    const bool a_row = o.layout_a == GEMM_ROW_MAJOR, b_row = o.layout_b == GEMM_ROW_MAJOR,
+               c_row = o.layout_c == GEMM_ROW_MAJOR;
+    if (ldc < (c_row ? N : M) || (K > 0 && (lda < (a_row ? K : M) || ldb < (b_row ? N : K))))
+        return fail(&h->err, GEMM_ERR_INVALID_ARG, "leading dimension smaller than the stored extent");
+    HostMat a{static_cast<const char*>(A), nullptr, a_row ? M : K, a_row ? K : M, lda, 2};
+    HostMat b{static_cast<const char*>(B), nullptr, b_row ? K : N, b_row ? N : K, ldb, 2};
+    HostMat c{static_cast<const char*>(C), nullptr, c_row ? M : N, c_row ? N : M, ldc, esc};
+    auto fp = [](const HostMat& m) -> int64_t { return m.outer == 0 || m.inner == 0 ? 0 : (m.outer - 1) * m.ld + m.inner; };
+    if (strideC < c.outer * ldc ||
+        (K > 0 && (strideA < 0 || strideB < 0 || (strideA != 0 && strideA < a.outer * lda) ||
+                   (strideB != 0 && strideB < b.outer * ldb))))
+        return fail(&h->err, GEMM_ERR_INVALID_ARG,
+                    "strides must keep the matrices apart (A and B may also use 0: one matrix for every product)");
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    struct Restore {
+        int d, p;
+        ~Restore() { if (d != p) cudaSetDevice(p); }
+    } restore{h->device, prev};
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+    const int64_t a_span = K > 0 ? (batch - 1) * strideA + fp(a) : 0;
+    const int64_t b_span = K > 0 ? (batch - 1) * strideB + fp(b) : 0;
+    const int64_t c_span = (batch - 1) * strideC + fp(c);
+    gemm_status_t s;
+    if ((s = ensure_stage(h, 0, (size_t)a_span * 2 + 16)) != GEMM_OK) return s;
+    if ((s = ensure_stage(h, 1, (size_t)b_span * 2 + 16)) != GEMM_OK) return s;
+    if ((s = ensure_stage(h, 2, (size_t)c_span * esc + 16)) != GEMM_OK) return s;
+    if ((s = pipe_setup(h)) != GEMM_OK) return s;
+    char* da = static_cast<char*>(h->stage_ptr[0]);
+    char* db = static_cast<char*>(h->stage_ptr[1]);
+    char* dc = static_cast<char*>(h->stage_ptr[2]);
+    const char* ha = static_cast<const char*>(A);
+    const char* hb = static_cast<const char*>(B);
+    char* hc = static_cast<char*>(C);
+
+    const int64_t want = o.host_parts > 0 ? o.host_parts : kHostChunks;
+    const int64_t step = (batch + std::min<int64_t>(want, batch) - 1) / std::min<int64_t>(want, batch);
+    const int64_t parts = (batch + step - 1) / step;
+    const bool a_whole = K > 0 && strideA == 0;         // one A for every product: copy it once
+    const bool b_whole = K > 0 && strideB == 0;
+    const bool c_dense = ldc == c.inner && strideC == fp(c);
+    // Bytes [first line of batch b0, end of batch b1 - 1) of an operand with stride st.
+    auto span_copy = [](char* dev, const char* host, int64_t st, int64_t foot, int esize, int64_t b0, int64_t b1,
+                        bool to_device, cudaStream_t cs) -> cudaError_t {
+        const size_t off = (size_t)(b0 * st) * esize;
+        const size_t bytes = (size_t)((b1 - 1 - b0) * st + foot) * esize;
+        return to_device ? cudaMemcpyAsync(dev + off, host + off, bytes, cudaMemcpyHostToDevice, cs)
+                         : cudaMemcpyAsync(const_cast<char*>(host) + off, dev + off, bytes, cudaMemcpyDeviceToHost, cs);
+    };
+
+    cudaError_t e = cudaEventRecord(h->ev_start, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->pipe_in, h->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->pipe_out, h->ev_start, 0);
+    if (e == cudaSuccess && a_whole) e = span_copy(da, ha, strideA, fp(a), 2, 0, batch, true, h->pipe_in);
+    if (e == cudaSuccess && b_whole) e = span_copy(db, hb, strideB, fp(b), 2, 0, batch, true, h->pipe_in);
+    for (int64_t i = 0; i < parts && e == cudaSuccess && s == GEMM_OK; ++i) {
+        const int64_t b0 = i * step, b1 = std::min(batch, b0 + step);
+        if (K > 0 && !a_whole) e = span_copy(da, ha, strideA, fp(a), 2, b0, b1, true, h->pipe_in);
+        if (e == cudaSuccess && K > 0 && !b_whole) e = span_copy(db, hb, strideB, fp(b), 2, b0, b1, true, h->pipe_in);
+        if (e == cudaSuccess && beta != 0.0f) e = span_copy(dc, hc, strideC, fp(c), esc, b0, b1, true, h->pipe_in);
+        if (e == cudaSuccess) e = cudaEventRecord(h->ev_in[i], h->pipe_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, h->ev_in[i], 0);
+        if (e != cudaSuccess) break;
+        s = run_impl(h, M, N, K, da + (size_t)(b0 * strideA) * 2, lda, strideA, db + (size_t)(b0 * strideB) * 2, ldb,
+                     strideB, dc + (size_t)(b0 * strideC) * esc, ldc, strideC, b1 - b0, alpha, beta, stream_v);
+        if (s != GEMM_OK) break;
+        e = cudaEventRecord(h->ev_c[i], stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->pipe_out, h->ev_c[i], 0);
+        if (c_dense) {
+            if (e == cudaSuccess) e = span_copy(dc, hc, strideC, fp(c), esc, b0, b1, false, h->pipe_out);
+        } else {
+            // Padding between lines or batches stays untouched on the host.
+            for (int64_t bb = b0; bb < b1 && e == cudaSuccess; ++bb) {
+                const size_t off = (size_t)(bb * strideC) * esc;
+                HostMat cb{hc + off, dc + off, c.outer, c.inner, ldc, esc};
+                e = copy_block(cb, 0, c.outer, 0, c.inner, false, h->pipe_out);
+            }
+        }
+    }
+    if (e == cudaSuccess && s == GEMM_OK) {
+        e = cudaEventRecord(h->ev_out_done, h->pipe_out);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, h->ev_out_done, 0);
+    }
     const cudaError_t e_in = cudaStreamSynchronize(h->pipe_in);
     const cudaError_t e_out = cudaStreamSynchronize(h->pipe_out);
     const cudaError_t e_s = cudaStreamSynchronize(stream);

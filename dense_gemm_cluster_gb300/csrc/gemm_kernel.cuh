@@ -97,6 +97,7 @@ struct KernelParams {
     float* workspace;        // one BLOCK_M x BN fp32 partial slot per CTA of the grid
     unsigned int* flags;     // per slot: 1 while the slot holds a partial not yet summed, else 0
     int clc;                 // 1: one cluster per tile; running clusters take pending ones' tiles
+    int a_shared, b_shared;  // 1: one matrix serves every product of the batch (stride 0)
 };
 
 struct TileCoord {
@@ -313,6 +314,7 @@ struct OperandPlan {
     int kmap4;             // K-major with the 4-D k-split map
     int slice, parts;      // this CTA's slice index and the group size
     uint32_t mask;         // receivers (multicast) or just this CTA
+    int shared;            // one matrix for the whole batch: batch coordinate 0
 };
 
 template <int G, int BK>
@@ -396,6 +398,7 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
             ++requests;
         }
         const TileCoord tc = tile_coord(p, t);
+        const int zb = op.shared ? 0 : tc.b;           // batch coordinate of this operand
         const int mn0 = is_a ? (tc.ctm * cx + rx) * BLOCK_M
                              : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -416,12 +419,12 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
             if (op.mn_major) {
                 const int y = kb * BK + op.slice * k_rows;
                 for (int box = 0; box < op.rows / 64; ++box)
-                    tma_issue<G, BK>(op, mcast, dst + (uint32_t)(box * BK * 128), bar, mn0 + box * 64, y, tc.b, 0,
+                    tma_issue<G, BK>(op, mcast, dst + (uint32_t)(box * BK * 128), bar, mn0 + box * 64, y, zb, 0,
                                      false);
             } else if (op.kmap4) {
-                tma_issue<G, BK>(op, mcast, dst, bar, 0, mn0 + r0, kb * NAT + atom0, tc.b, true);
+                tma_issue<G, BK>(op, mcast, dst, bar, 0, mn0 + r0, kb * NAT + atom0, zb, true);
             } else {
-                tma_issue<G, BK>(op, mcast, dst, bar, kb * BK, mn0 + r0, tc.b, 0, false);
+                tma_issue<G, BK>(op, mcast, dst, bar, kb * BK, mn0 + r0, zb, 0, false);
             }
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -731,10 +734,12 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             OperandPlan op;
             if (is_a) {
                 prefetch_tmap(&tmA);
-                op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, p.a_kmap4, idxA, gA, maskA};
+                op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, p.a_kmap4, idxA, gA, maskA,
+                                 p.a_shared};
             } else {
                 prefetch_tmap(&tmB);
-                op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB};
+                op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB,
+                                 p.b_shared};
             }
             produce<G, BK>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
                        BN, BN_CTA, abort_flag, cluster, clusters, S, &clc_ctx, smem_u32(&ring_empty[0]));

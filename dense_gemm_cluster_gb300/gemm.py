@@ -68,6 +68,9 @@ _lib.gemm_run_strided_batched.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64
 _lib.gemm_run_strided_batched.restype = _i32
 _lib.gemm_run_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32, _f32, _vp]
 _lib.gemm_run_host.restype = _i32
+_lib.gemm_run_strided_batched_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64,
+                                               _i64, _i64, _f32, _f32, _vp]
+_lib.gemm_run_strided_batched_host.restype = _i32
 _lib.gemm_query_status.argtypes = [_vp, _vp]
 _lib.gemm_query_status.restype = _i32
 _lib.gemm_plan.argtypes = [_OPT_P, _i64, _i64, _i64, _i64, _i32, ctypes.POINTER(gemm_plan_t)]
@@ -131,6 +134,12 @@ def gemm_run_strided_batched(h, M, N, K, A, lda, strideA, B, ldb, strideB, C, ld
                              alpha, beta, stream=None) -> int:
     return _lib.gemm_run_strided_batched(h, M, N, K, _ptr(A), lda, strideA, _ptr(B), ldb, strideB, _ptr(C),
                                          ldc, strideC, batch, alpha, beta, _stream(stream))
+
+
+def gemm_run_strided_batched_host(h, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch, alpha, beta,
+                                  stream=None) -> int:
+    return _lib.gemm_run_strided_batched_host(h, M, N, K, _ptr(A), lda, sA, _ptr(B), ldb, sB, _ptr(C), ldc, sC, batch,
+                                              alpha, beta, _stream(stream))
 
 
 def gemm_run_host(h, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream=None) -> int:
@@ -216,6 +225,11 @@ class Gemm:
 
     def run_host(self, M, N, K, A, lda, B, ldb, C, ldc, alpha=1.0, beta=0.0, stream=None) -> None:
         self.check(gemm_run_host(self.handle, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream))
+
+    def run_strided_batched_host(self, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch, alpha=1.0, beta=0.0,
+                                 stream=None) -> None:
+        self.check(gemm_run_strided_batched_host(self.handle, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch,
+                                                 alpha, beta, stream))
 
     def query_status(self, stream=None) -> int:
         return gemm_query_status(self.handle, stream)

@@ -154,8 +154,10 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                        void *C, int64_t ldc, float alpha, float beta, void *stream);
 
 /* `batch` independent products C[i] <- alpha*A[i]*B[i] + beta*C[i], where X[i]
- * starts strideX elements after X[i-1]. Strides must be multiples of 16 bytes;
- * strideC must not make two outputs overlap. The attention-score form is
+ * starts strideX elements after X[i-1]. Strides must be multiples of 16 bytes
+ * and keep the matrices apart (at least ld x the stored outer extent), except
+ * that strideA or strideB may be 0: one matrix serves every product. Overlapping
+ * strides return GEMM_ERR_INVALID_ARG. The attention-score form is
  * A = Q (row-major, sq x d), B = K^T (K given row-major sk x d is B column-major
  * with ldb = d), C = S (fp32, sq x sk). */
 gemm_status_t gemm_run_strided_batched(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
@@ -178,6 +180,20 @@ gemm_status_t gemm_run_strided_batched(gemm_handle_t h, int64_t M, int64_t N, in
 gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                             const void *A, int64_t lda, const void *B, int64_t ldb,
                             void *C, int64_t ldc, float alpha, float beta, void *stream);
+
+/* gemm_run_strided_batched on HOST buffers, copied through the handle's staging
+ * like gemm_run_host: the batch is split into up to 8 parts of whole products
+ * (options.host_parts caps the count), part i's A, B (and C when beta != 0)
+ * copied in while part i-1 runs and part i-2's C is copied out. An operand with
+ * stride 0 (one matrix for every product) is copied once, first. C comes back line
+ * by line unless its batches and lines are
+ * dense, so no padding is written on the host. batch = 1 is gemm_run_host.
+ * Synchronizes `stream` before returning. */
+gemm_status_t gemm_run_strided_batched_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                            const void *A, int64_t lda, int64_t strideA,
+                                            const void *B, int64_t ldb, int64_t strideB,
+                                            void *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                            float alpha, float beta, void *stream);
 
 /* Synchronizes `stream`, then reads and clears the device status word.
  * GEMM_ERR_DEVICE_TIMEOUT if a bounded wait expired in any run since the last

@@ -116,3 +116,40 @@ def test_attention_workload_full_size_sampled():
         got_lse = lse[b, torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
         assert np.max(np.abs(got - ref[0])) <= 1e-2 * vmax, f"head {b}"
         assert np.max(np.abs(got_lse - ref_lse[0]) / (1.0 + np.abs(ref_lse[0]))) <= 1e-4, f"head {b}"
+
+
+@pytest.mark.parametrize("opts", [dict(mode="mcast", mcast_b=1, cluster_m=2),
+                                  dict(cta_group=2, cluster_m=2, schedule="stream_k")])
+def test_output_past_2_31_elements(opts):
+    # One C of 131272 x 16512 bf16 (2.17e9 elements, more rows than a 16-bit coordinate):
+    # element offsets past 2^31 in the beta * C_in reads, the TMA stores and (stream-K)
+    # the partial slots. C_in is the pattern c[i, j] = ((i mod 61) - 30 - (j mod 53)) / 16,
+    # exact in bf16 and known at every position, so the expected value is the oracle's
+    # product plus beta times the pattern.
+    import torch
+    import oracle
+    from dense_gemm_cluster_gb300 import gemm, inputs
+    M, N, K, beta = 131272, 16512, 128, 0.5
+    A, lda = inputs.store(inputs.bf16_matrix(M, K, "normal", 51), "row")
+    B, ldb = inputs.store(inputs.bf16_matrix(K, N, "normal", 52), "row")
+    pattern = lambda i, j: ((i % 61) - 30.0 - (j % 53)) / 16.0
+    ri = torch.arange(M, device="cuda", dtype=torch.float32).view(M, 1)
+    cj = torch.arange(N, device="cuda", dtype=torch.float32).view(1, N)
+    dC = ((ri.remainder(61) - 30.0) - cj.remainder(53)).mul_(1.0 / 16.0).to(torch.bfloat16).view(-1)
+    g = gemm.Gemm(0, layout_a="row", layout_b="row", layout_c="row", out_type="bf16", **opts)
+    try:
+        g.run(M, N, K, torch_dev(A), lda, torch_dev(B), ldb, dC, N, 1.0, beta)
+        assert g.query_status() == 0
+    finally:
+        g.close()
+    rows, cols = sample_positions(M, N, 2000, seed=3)
+    rng = np.random.default_rng(4)
+    far = int(2 ** 31 // N) + 1                  # rows whose every element lies past 2^31
+    rows = np.concatenate([rows, rng.integers(far, M, 500), [M - 1, far]])
+    cols = np.concatenate([cols, rng.integers(0, N, 500), [N - 1, 0]])
+    flat = torch.from_numpy(rows * N + cols).cuda()
+    got = inputs.bf16_bits_to_f32(dC.view(torch.int16)[flat].cpu().numpy().view(np.uint16)).astype(np.float64)
+    ref = oracle.gemm_entries(rows, cols, K, A, lda, "row", B, ldb, "row") + beta * pattern(rows, cols)
+    _check_sampled(got, ref, K, "bf16", f"2^31+ elements {opts}")
+    del dC
+    torch.cuda.empty_cache()

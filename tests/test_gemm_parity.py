@@ -5,7 +5,7 @@ cta_group 1 here (unicast and cluster multicast); the pair MMA has its own file.
 import numpy as np
 import pytest
 
-from gpu_cases import Problem, assert_close, options_for, sample_positions
+from gpu_cases import Problem, assert_close, decode, options_for, sample_positions
 
 pytestmark = pytest.mark.gpu
 
@@ -209,3 +209,40 @@ def test_gemm_replays_in_a_cuda_graph(G, opts):
         assert g.query_status() == G.GEMM_OK
     finally:
         g.close()
+
+
+@pytest.mark.parametrize("shared", ["A", "B"])
+@pytest.mark.parametrize("opts", [dict(), dict(mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2),
+                                  dict(cta_group=2, cluster_m=2)])
+def test_batch_stride_zero_shares_one_matrix(G, shared, opts):
+    # strideA (or strideB) = 0: every product of the batch reads the same matrix.
+    import torch
+    from gpu_cases import torch_dev
+    M, N, K, batch = 300, 260, 192, 3
+    probs = [Problem(M, N, K, la="row", lb="col", out="f32", seed=70 + i) for i in range(batch)]
+    for p in probs[1:]:
+        if shared == "A":
+            p.A = probs[0].A
+        else:
+            p.B = probs[0].B
+    A = np.concatenate([probs[0].A.reshape(-1)] if shared == "A" else [p.A.reshape(-1) for p in probs])
+    B = np.concatenate([probs[0].B.reshape(-1)] if shared == "B" else [p.B.reshape(-1) for p in probs])
+    sA = 0 if shared == "A" else probs[0].A.size
+    sB = 0 if shared == "B" else probs[0].B.size
+    lda, ldb, ldc = probs[0].lda, probs[0].ldb, probs[0].ldc
+    sC = probs[0].C_in.size
+    dC = torch.full((batch * sC,), float("nan"), dtype=torch.float32, device="cuda")
+    g = G.Gemm(0, **options_for(probs[0], **opts))
+    try:
+        g.run_strided_batched(M, N, K, torch_dev(A), lda, sA, torch_dev(B), ldb, sB, dC, ldc, sC, batch)
+        assert g.query_status() == G.GEMM_OK
+        # overlapping (non-zero, shorter than one matrix) strides are refused before any launch
+        s = G.gemm_run_strided_batched(g.handle, M, N, K, torch_dev(A), lda, 16, torch_dev(B), ldb, sB, dC, ldc, sC,
+                                       batch, 1.0, 0.0)
+        assert s == G.GEMM_ERR_INVALID_ARG
+    finally:
+        g.close()
+    out = dC.cpu().numpy()
+    for i, p in enumerate(probs):
+        assert_close(decode(out[i * sC:(i + 1) * sC].reshape(M, ldc), M, N, "row"), p.reference(), K, "f32",
+                     f"stride 0 on {shared}, product {i}")

@@ -94,3 +94,61 @@ def test_host_entry_repeats_on_one_handle(G):
             assert_close(decode(C, M, N, "row"), p.reference(), K, "f32", f"repeat {M}x{N}x{K}")
     finally:
         g.close()
+
+
+def _batched_case(batch, M, N, K, la, lb, lc, out, beta, seed, a_stride_pad=0, c_extra=0, share_a=False):
+    """Per-batch problems stored at strides (padding between batches and lines); returns buffers and refs."""
+    probs = [Problem(M, N, K, la=la, lb=lb, lc=lc, out=out, beta=beta, seed=seed + 7 * i) for i in range(batch)]
+    if share_a:
+        for p in probs[1:]:
+            p.A_log, p.A, p.lda = probs[0].A_log, probs[0].A, probs[0].lda
+    p0 = probs[0]
+    lda, ldb = p0.lda, p0.ldb
+    ldc = pad_ld(N if lc == "row" else M) if c_extra else p0.ldc
+    a_elems, b_elems = p0.A.size, p0.B.size
+    c_outer = M if lc == "row" else N
+    sA = 0 if share_a else a_elems + a_stride_pad
+    sB = b_elems
+    sC = c_outer * ldc + c_extra
+    A = np.zeros(max(1, (batch - 1) * sA + a_elems), np.uint16)
+    B = np.zeros((batch - 1) * sB + b_elems, np.uint16)
+    cdt = np.uint16 if out == "bf16" else np.float32
+    C = np.full((batch - 1) * sC + c_outer * ldc, SENTINEL_BF16 if out == "bf16" else SENTINEL_F32, cdt)
+    refs = []
+    c_inner = N if lc == "row" else M
+    for i, p in enumerate(probs):
+        A[i * sA:i * sA + a_elems] = p.A.reshape(-1)
+        B[i * sB:i * sB + b_elems] = p.B.reshape(-1)
+        c_log = p.C_in[:, :c_inner] if lc == "row" else p.C_in[:, :c_inner].T
+        cb, _ = inputs.store(np.ascontiguousarray(c_log), lc, ldc)
+        view = C[i * sC:i * sC + c_outer * ldc].reshape(c_outer, ldc)
+        view[:, :c_inner] = cb[:, :c_inner]
+        p.C_in, p.ldc = cb, ldc
+        refs.append(p.reference(1.0, beta))
+    return A, lda, sA, B, ldb, sB, C, ldc, sC, refs, c_inner, c_outer
+
+
+@pytest.mark.parametrize("batch,M,N,K,la,lb,lc,out,beta,opts,extra", [
+    (12, 300, 200, 128, "row", "col", "row", "f32", 0.0, dict(host_parts=4), {}),     # the score form, dense
+    (7, 260, 300, 192, "row", "row", "row", "bf16", 0.5, dict(mode="mcast", mcast_b=1, cluster_m=2),
+     dict(a_stride_pad=64, c_extra=40)),                                               # padded batches and lines
+    (5, 256, 384, 64, "col", "col", "col", "f32", 0.5, dict(cta_group=2, cluster_n=2, host_parts=2),
+     dict(share_a=True, c_extra=8)),                                                   # one A for every product
+    (1, 300, 200, 128, "row", "col", "row", "bf16", 0.0, dict(), {}),                  # batch 1: gemm_run_host
+])
+def test_batched_host_entry_matches_oracle(G, batch, M, N, K, la, lb, lc, out, beta, opts, extra):
+    A, lda, sA, B, ldb, sB, C, ldc, sC, refs, c_inner, c_outer = _batched_case(batch, M, N, K, la, lb, lc, out,
+                                                                                beta, 60, **extra)
+    g = G.Gemm(0, layout_a=la, layout_b=lb, layout_c=lc, out_type=out, **opts)
+    try:
+        g.run_strided_batched_host(M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch, 1.0, beta)
+        assert g.query_status() == G.GEMM_OK
+    finally:
+        g.close()
+    sentinel = SENTINEL_BF16 if out == "bf16" else SENTINEL_F32
+    for i in range(batch):
+        view = C[i * sC:i * sC + c_outer * ldc].reshape(c_outer, ldc)
+        assert_close(decode(view, M, N, lc), refs[i], K, out, f"batched host entry, product {i}")
+        assert (view[:, c_inner:] == sentinel).all(), "line padding written"
+        if i + 1 < batch:
+            assert (C[i * sC + c_outer * ldc:(i + 1) * sC] == sentinel).all(), "padding between products written"
