@@ -710,6 +710,13 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tmem_alloc<G>(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish<G>();
     }
+    if (warp == 6 && lane == 0) {
+        // Fetch the descriptors while thread 0 initialises the barriers, so the first
+        // loads do not wait for them after the cluster barrier.
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
+    }
     tc_fence_before();
     __syncthreads();
     cluster_sync();
