@@ -596,11 +596,17 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     const int cs = pl.cluster_m * pl.cluster_n;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: this grid may be scheduled while the previous
+    // kernel in the stream finishes; the kernel waits for that kernel's completion
+    // (griddepcontrol.wait) before its first global memory access. Not with cluster
+    // launch control, whose pending clusters must not compete with a next grid.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(dgc::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = stream;
@@ -653,6 +659,7 @@ static gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
         kp.workspace = h->workspace;
         kp.flags = h->flags;
     }
+    cfg.numAttrs = o.schedule == 3 ? 1 : 2;
     void* args[] = {&tmA, &tmB, &tmC, &kp};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "cudaLaunchKernelEx: %s", cudaGetErrorString(e));

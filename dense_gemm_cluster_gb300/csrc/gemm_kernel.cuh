@@ -722,6 +722,12 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Programmatic dependent launch: let the next grid in the stream be scheduled,
+    // and touch no global memory (operands, C, workspace, flags, status) before the
+    // previous grid has completed and its writes are visible. Both are no-ops for a
+    // launch without the attribute.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const long long cluster = cluster_id_x();
     const long long clusters = num_clusters_x();
