@@ -7,10 +7,11 @@ and L2->SM operand bytes against unicast.
 
 One step is one gemm_run over the workload (default: GEMM 4096^3, bf16 in,
 bf16 out, 2x1 cluster multicasting A and B). Inputs are seeded synthetic
-matrices resident in HBM. When they fit in L2 it is flushed (a 512 MB write,
-then a read) before every timed step and each step is timed alone with CUDA
-events on the launching stream; larger inputs need no flush and the K steps
-run back to back between one pair of events.
+matrices resident in HBM. Inputs that fit in L2 are rotated through copies
+that together exceed twice L2 (so no step finds its operands in L2), or for
+tiny problems L2 is flushed (a 512 MB write, then a read) before every step
+and each step is timed alone with CUDA events on the launching stream;
+otherwise the K steps run back to back between one pair of events.
 Prints one JSON line (rank 0).
 
 --impl reference times the CPU oracle (fp64 triple loop, OpenMP) on a bounded
@@ -43,6 +44,7 @@ METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense-BF16 peak; L2→SM bytes vs uni
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 129 << 20          # GB300 L2 (126 MiB usable); inputs above this need no flush
+MAX_ROTATION = 8              # most copies of a workload's buffers the bench rotates through instead of a flush
 KERNEL_SOURCES = ["dense_gemm_cluster_gb300/csrc/gemm_kernel.cuh", "dense_gemm_cluster_gb300/csrc/ptx.cuh",
                   "dense_gemm_cluster_gb300/csrc/gemm_host.cu"]
 ATTN_KERNEL_SOURCES = ["dense_gemm_cluster_gb300/csrc/attention.cu", "dense_gemm_cluster_gb300/csrc/ptx.cuh"]
@@ -228,6 +230,13 @@ class DeviceProblem:
             self.C = torch.empty(c_elems, dtype=cdt, device=device)
         self.c_bytes = c_elems * esc
 
+    def replica(self):
+        """Another device copy of the operands and C (same values), for rotating through steps."""
+        import copy
+        r = copy.copy(self)
+        r.A, r.B, r.C = self.A.clone(), self.B.clone(), self.C.clone()
+        return r
+
 
 def run_once(g, p: DeviceProblem, stream):
     w = p.w
@@ -347,14 +356,25 @@ def bench_ours(args, w: Workload):
     p = DeviceProblem(w, device)
     stream = torch.cuda.current_stream(device)
     input_bytes = w.min_hbm_bytes()
-    needs_flush = input_bytes <= L2_BYTES
+    # Inputs that fit in L2 must not be served from it: steps rotate through enough
+    # copies of the operands and C that the others' traffic between two uses of a
+    # copy is more than twice L2; when that takes too many copies, L2 is flushed
+    # before every step instead.
+    copies = [p]
+    needs_flush = False
+    if input_bytes <= L2_BYTES:
+        rot = -(-2 * L2_BYTES // input_bytes) + 1
+        if rot <= MAX_ROTATION:
+            copies += [p.replica() for _ in range(rot - 1)]
+        else:
+            needs_flush = True
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device) if needs_flush else None
     # A read after the write leaves L2 holding clean lines, so the timed kernel
     # does not pay for writing back the flush buffer.
     clean = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=device) if needs_flush else None
 
-    for _ in range(max(3, args.warmup)):
-        run_once(g, p, stream)
+    for i in range(max(3, args.warmup, len(copies))):
+        run_once(g, copies[i % len(copies)], stream)
     g.check(g.query_status(stream))
 
     # With an L2 flush between steps each step is bracketed by its own events (the
@@ -375,7 +395,7 @@ def bench_ours(args, w: Workload):
                 flush.fill_(float(i))                  # evicts the operands from L2
                 clean.sum()
                 starts[i].record(stream)
-            run_once(g, p, stream)
+            run_once(g, copies[i % len(copies)], stream)
             if needs_flush:
                 ends[i].record(stream)
         if not needs_flush:
@@ -431,8 +451,11 @@ def bench_ours(args, w: Workload):
                    "l2": (f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB write, then a "
                           f"{L2_FLUSH_BYTES >> 21} MB read), each step between its own pair of events"
                           if needs_flush else
-                          f"no flush: the inputs ({input_bytes >> 20} MB) are larger than L2; the K steps run "
-                          f"back to back between one pair of events"),
+                          (f"no flush: the steps rotate through {len(copies)} copies of the operands and C "
+                           f"({(len(copies) * input_bytes) >> 20} MB, more than twice L2 between two uses of a copy); "
+                           f"the K steps run back to back between one pair of events" if len(copies) > 1 else
+                           f"no flush: the inputs ({input_bytes >> 20} MB) are larger than L2; the K steps run "
+                           f"back to back between one pair of events")),
                    "description": w.description},
         "roofline": roofline,
         "l2_to_sm_operand_bytes": {"analytic": plan.l2_to_sm_operand_bytes,
