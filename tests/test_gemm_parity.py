@@ -246,3 +246,46 @@ def test_batch_stride_zero_shares_one_matrix(G, shared, opts):
     for i, p in enumerate(probs):
         assert_close(decode(out[i * sC:(i + 1) * sC].reshape(M, ldc), M, N, "row"), p.reference(), K, "f32",
                      f"stride 0 on {shared}, product {i}")
+
+
+@pytest.mark.parametrize("opts", [dict(mode="mcast", mcast_b=1, cluster_m=2),
+                                  dict(schedule="stream_k", max_clusters=7, block_n=128),
+                                  dict(cta_group=2, cluster_m=2)])
+def test_back_to_back_launches_read_the_previous_result(G, opts):
+    # Launches overlap their prologue with the previous kernel (programmatic dependent
+    # launch); each must still read what the previous one wrote. A chain of GEMMs, each
+    # taking the previous output as its A, runs once back to back on one stream and once
+    # with a device synchronisation between launches: the results must be bitwise equal.
+    import torch
+    from gpu_cases import torch_dev
+    M, K = 700, 512
+    dims = [512, 384, 640, 512]
+    Bs = [torch_dev(inputs_bf16(K if i == 0 else dims[i - 1], dims[i], 90 + i)) for i in range(len(dims))]
+    A0 = torch_dev(inputs_bf16(M, K, 89))
+
+    def chain(sync):
+        g = G.Gemm(0, layout_a="row", layout_b="row", layout_c="row", out_type="bf16", **opts)
+        try:
+            a, outs = A0, []
+            for i, b in enumerate(Bs):
+                k = K if i == 0 else dims[i - 1]
+                c = torch.empty(M * dims[i], dtype=torch.int16, device="cuda")
+                g.run(M, dims[i], k, a, k, b, dims[i], c, dims[i], 1.0 / 16.0, 0.0)
+                if sync:
+                    torch.cuda.synchronize()
+                outs.append(c)
+                a = c
+            assert g.query_status() == G.GEMM_OK
+        finally:
+            g.close()
+        return [o.cpu().numpy() for o in outs]
+
+    for x, y in zip(chain(False), chain(True)):
+        assert np.array_equal(x, y)
+    assert np.isfinite(decode(chain(False)[-1].view(np.uint16).reshape(M, dims[-1]), M, dims[-1], "row")).all()
+
+
+def inputs_bf16(rows, cols, seed):
+    from dense_gemm_cluster_gb300 import inputs
+    buf, _ = inputs.store(inputs.bf16_matrix(rows, cols, "normal", seed), "row")
+    return buf
