@@ -83,7 +83,7 @@ __device__ bool attn_wait(uint32_t bar, uint32_t parity, const AttnParams& p, ui
         if (clock_cycles() - c0 > 2ull * p.timeout_ns) {
             if (atomicCAS(&g_attn_status[0], 0u, code) == 0u) {
                 g_attn_status[1] = blockIdx.x;
-                g_attn_status[2] = blockIdx.y;
+                g_attn_status[2] = blockIdx.z * gridDim.y + blockIdx.y;
                 __threadfence();
             }
             return false;
@@ -102,7 +102,7 @@ __device__ bool attn_wait_cluster(uint32_t bar, uint32_t parity, const AttnParam
         if (clock_cycles() - c0 > 2ull * p.timeout_ns) {
             if (atomicCAS(&g_attn_status[0], 0u, code) == 0u) {
                 g_attn_status[1] = blockIdx.x;
-                g_attn_status[2] = blockIdx.y;
+                g_attn_status[2] = blockIdx.z * gridDim.y + blockIdx.y;
                 __threadfence();
             }
             return false;
@@ -154,7 +154,10 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int c = p.cluster;
     const uint32_t rank = c > 1 ? cluster_ctarank() : 0u;
     const uint16_t all = (uint16_t)((1u << c) - 1u);
-    const int b = blockIdx.y;
+    // Heads: grid y, continued in grid z past 65535 (a cluster spans grid x only, so
+    // a whole cluster leaves together when the last z slice runs past the batch).
+    const int b = (int)(blockIdx.z * gridDim.y + blockIdx.y);
+    if (b >= p.batch) return;
     const int q0 = blockIdx.x * (QT * TQ);
 
     if (threadIdx.x == 0) {
@@ -528,7 +531,7 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
          reinterpret_cast<uintptr_t>(O) | reinterpret_cast<uintptr_t>(lse)) & 15u)
         return afail(GEMM_ERR_ALIGNMENT, "Q, K, V, O and lse must be 16-byte aligned");
-    if (batch >= 65536 || sq >= (1ll << 31) || sk >= (1ll << 31)) return afail(GEMM_ERR_INVALID_ARG, "too large");
+    if (batch >= (1ll << 31) || sq >= (1ll << 31) || sk >= (1ll << 31)) return afail(GEMM_ERR_INVALID_ARG, "too large");
     auto enc = attn_encoder();
     if (!enc) return afail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     CUtensorMap tq, tk, tv;
@@ -583,7 +586,8 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     attr[0].val.clusterDim.x = cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)ctas, (unsigned)batch, 1);
+    const unsigned gy = (unsigned)(batch < 65535 ? batch : 65535);
+    cfg.gridDim = dim3((unsigned)ctas, gy, (unsigned)((batch + gy - 1) / gy));
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = static_cast<cudaStream_t>(stream);

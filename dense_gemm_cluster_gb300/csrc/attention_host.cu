@@ -81,7 +81,7 @@ extern "C" gemm_status_t attention_forward_run_host(const void* Q, const void* K
                                                     size_t workspace_bytes, void* stream_v) {
     if (batch < 0 || sq < 0 || sk < 0) return GEMM_ERR_INVALID_ARG;
     if (batch == 0 || sq == 0) return GEMM_OK;
-    if (sk == 0 || batch >= 65536 || sq >= (1ll << 31) || sk >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
+    if (sk == 0 || batch >= (1ll << 31) || sq >= (1ll << 31) || sk >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
     if (d != 128 || (cluster != 1 && cluster != 2 && cluster != 4) || (cta_group != 1 && cta_group != 2) ||
         (cta_group == 2 && cluster != 2))
         return GEMM_ERR_UNSUPPORTED;

@@ -184,7 +184,7 @@ def test_attention_validation_before_launch(lib):
     assert run(None, a, a, a, None, 1, 128, 128, 128) == lib.GEMM_ERR_INVALID_ARG
     assert run(m, a, a, a, None, 1, 128, 128, 128) == lib.GEMM_ERR_ALIGNMENT
     assert run(a, a, a, a, m, 1, 128, 128, 128) == lib.GEMM_ERR_ALIGNMENT               # lse
-    assert run(a, a, a, a, None, 1 << 16, 128, 128, 128) == lib.GEMM_ERR_INVALID_ARG      # batch limit
+    assert run(a, a, a, a, None, 1 << 31, 128, 128, 128) == lib.GEMM_ERR_INVALID_ARG      # batch limit
     assert run(a, a, a, a, None, 0, 128, 128, 128) == lib.GEMM_OK                         # nothing to do
     assert run(a, a, a, a, None, 3, 0, 128, 128) == lib.GEMM_OK
     # the host-buffer entry point checks its workspace and arguments before any copy

@@ -189,3 +189,25 @@ def test_attention_host_entry_equals_device_entry(b, sq, sk, cluster, cta_group,
     assert np.array_equal(O_h.reshape(b, sq, 128).astype(np.float64), ref_o)
     if with_lse:
         assert np.array_equal(lse_h.reshape(b, sq).astype(np.float64), ref_lse)
+
+
+def test_attention_more_heads_than_one_grid_dimension_holds():
+    # 70000 heads of 8 queries and 8 keys: the heads continue in grid z past 65535.
+    import torch
+    import oracle
+    from dense_gemm_cluster_gb300 import gemm, inputs
+    b, sq, sk = 70000, 8, 8
+    Q, K, V = _inputs(b, sq, sk, 500)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+    O = torch.full((b * sq * 128,), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((b * sq,), float("nan"), dtype=torch.float32, device="cuda")
+    assert gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, 128, 0.0, 1, 2, 1) == gemm.GEMM_OK
+    assert gemm.attention_forward_query_status() == gemm.GEMM_OK
+    o = O.cpu().numpy().reshape(b, sq, 128).astype(np.float64)
+    l = lse.cpu().numpy().reshape(b, sq).astype(np.float64)
+    assert np.isfinite(o).all() and np.isfinite(l).all()
+    heads = np.array([0, 1, 65534, 65535, 65536, 69999])
+    ref, ref_lse = oracle.attention_forward(Q[heads], K[heads], V[heads], with_lse=True)
+    vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V[heads]))))
+    assert np.max(np.abs(o[heads] - ref)) <= 1e-2 * vmax
+    assert np.max(np.abs(l[heads] - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
