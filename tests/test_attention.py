@@ -42,7 +42,8 @@ def _run(Q, K, V, cluster, out_f32=0, scale=0.0, cta_group=1):
 MODES = [(1, 1), (2, 1), (4, 1), (2, 2)]          # (cluster, cta_group)
 
 
-@pytest.mark.parametrize("b,sq,sk", [(2, 128, 128), (3, 300, 500), (1, 1000, 130), (2, 256, 2048), (1, 77, 1)])
+@pytest.mark.parametrize("b,sq,sk", [(2, 128, 128), (3, 300, 500), (1, 1000, 130), (2, 256, 2048), (1, 77, 1),
+                                    (3, 1, 1), (2, 1, 300), (1, 257, 129)])
 @pytest.mark.parametrize("cluster,cta_group", MODES)
 def test_attention_matches_oracle(b, sq, sk, cluster, cta_group):
     import oracle

@@ -289,3 +289,16 @@ def inputs_bf16(rows, cols, seed):
     from dense_gemm_cluster_gb300 import inputs
     buf, _ = inputs.store(inputs.bf16_matrix(rows, cols, "normal", seed), "row")
     return buf
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 700, 96), (700, 1, 96), (5, 3, 4100), (2, 2, 8)])
+@pytest.mark.parametrize("opts", [dict(mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2),
+                                  dict(cta_group=2, cluster_m=4, mode="mcast", mcast_b=1),
+                                  dict(mode="mcast", mcast_b=1, cluster_m=8),
+                                  dict(schedule="clc", mode="mcast", mcast_a=1, cluster_n=2)])
+def test_degenerate_shapes_in_every_sharing_mode(G, M, N, K, opts):
+    # One row, one column, or a tiny output with a long K: a cluster's other CTAs (and a
+    # pair's odd CTA) hold only out-of-range rows and columns and must still take part.
+    p = Problem(M, N, K, la="row", lb="col", out="f32", beta=0.5, seed=80)
+    got = _run(G, p, 1.0, 0.5, **opts)
+    assert_close(got, p.reference(1.0, 0.5), K, "f32", f"{M}x{N}x{K} {opts}")
