@@ -302,3 +302,19 @@ def test_degenerate_shapes_in_every_sharing_mode(G, M, N, K, opts):
     p = Problem(M, N, K, la="row", lb="col", out="f32", beta=0.5, seed=80)
     got = _run(G, p, 1.0, 0.5, **opts)
     assert_close(got, p.reference(1.0, 0.5), K, "f32", f"{M}x{N}x{K} {opts}")
+
+
+@pytest.mark.parametrize("K,stages,out", [
+    (8192, 2, "bf16"),    # one tile over 8 clusters: 7 partials do not fit in the staging region
+    (3072, 2, "bf16"),    # 2 partials staged one column chunk per pass
+    (3072, 4, "f32"),     # 2 partials staged 6 column chunks, then 2
+])
+def test_stream_k_finisher_staging_paths(G, K, stages, out):
+    # A sub-wave problem: one 128 x 256 tile whose k-blocks are split over several
+    # clusters; the finisher adds the others' partials from staged shared memory, a
+    # pass at a time, or straight from global memory when they do not fit.
+    p = Problem(128, 256, K, la="row", lb="col", out=out, beta=0.5, seed=85)
+    a = _run(G, p, 1.0, 0.5, stages=stages)
+    b = _run(G, p, 1.0, 0.5, stages=stages)
+    assert_close(a, p.reference(1.0, 0.5), K, out, f"finisher staging K={K} stages={stages}")
+    assert np.array_equal(a, b)
