@@ -59,7 +59,7 @@ def _load():
             lib.oracle_gemm_entries.restype = i32
             lib.oracle_attention_scores.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp]
             lib.oracle_attention_scores.restype = i32
-            lib.oracle_attention_forward.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp, f64, vp, vp]
+            lib.oracle_attention_forward.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp, f64, i32, vp, vp]
             lib.oracle_attention_forward.restype = i32
             lib.oracle_stencil_1d.argtypes = [i64, vp, vp]
             lib.oracle_stencil_1d.restype = i32
@@ -149,9 +149,10 @@ def stencil_1d(x):
     return y
 
 
-def attention_forward(Q, Kmat, V, scale=None, with_lse=False):
+def attention_forward(Q, Kmat, V, scale=None, with_lse=False, causal=False):
     """O = softmax(scale Q K^T) V per batch for bf16-bit arrays Q (b, sq, d), K (b, sk, d),
-    V (b, sk, dv); float64 out (and the row log-sum-exp when with_lse). scale defaults to 1/sqrt(d)."""
+    V (b, sk, dv); float64 out (and the row log-sum-exp when with_lse). scale defaults to 1/sqrt(d).
+    causal: query i attends keys 0..i only (the others take no part in its softmax)."""
     Q = np.ascontiguousarray(Q, dtype=np.uint16)
     Kmat = np.ascontiguousarray(Kmat, dtype=np.uint16)
     V = np.ascontiguousarray(V, dtype=np.uint16)
@@ -164,7 +165,7 @@ def attention_forward(Q, Kmat, V, scale=None, with_lse=False):
     O = np.empty((b, sq, dv), dtype=np.float64)
     lse = np.empty((b, sq), dtype=np.float64)
     rc = _load().oracle_attention_forward(b, sq, sk, d, dv, _ptr(Q), _ptr(Kmat), _ptr(V), float(scale),
-                                          _ptr(O), _ptr(lse))
+                                          1 if causal else 0, _ptr(O), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_attention_forward rejected its arguments (code {rc})")
     return (O, lse) if with_lse else O

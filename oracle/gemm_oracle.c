@@ -177,7 +177,7 @@ int oracle_stencil_1d(int64_t n, const float *x, double *y)
  */
 int oracle_attention_forward(int64_t batch, int64_t sq, int64_t sk, int64_t d, int64_t dv,
                              const uint16_t *Q, const uint16_t *Kmat, const uint16_t *V,
-                             double scale, double *O, double *lse)
+                             double scale, int causal, double *O, double *lse)
 {
     if (batch < 0 || sq < 0 || sk < 1 || d < 0 || dv < 0)
         return 1;
@@ -188,7 +188,9 @@ int oracle_attention_forward(int64_t batch, int64_t sq, int64_t sk, int64_t d, i
             double *o = O + (b * sq + i) * dv;
             double *s = (double *)malloc(sizeof(double) * (size_t)sk);
             double m = -HUGE_VAL;
-            for (int64_t j = 0; j < sk; ++j) {
+            /* causal: query i sees keys 0..i only (the others are left out of the softmax) */
+            const int64_t nk = causal ? (i + 1 < sk ? i + 1 : sk) : sk;
+            for (int64_t j = 0; j < nk; ++j) {
                 const uint16_t *kr = Kmat + (b * sk + j) * d;
                 double acc = 0.0;
                 for (int64_t t = 0; t < d; ++t)
@@ -198,13 +200,13 @@ int oracle_attention_forward(int64_t batch, int64_t sq, int64_t sk, int64_t d, i
                     m = s[j];
             }
             double l = 0.0;
-            for (int64_t j = 0; j < sk; ++j) {
+            for (int64_t j = 0; j < nk; ++j) {
                 s[j] = exp(s[j] - m);
                 l += s[j];
             }
             for (int64_t c = 0; c < dv; ++c) {
                 double acc = 0.0;
-                for (int64_t j = 0; j < sk; ++j)
+                for (int64_t j = 0; j < nk; ++j)
                     acc += s[j] * bf16_to_double(V[(b * sk + j) * dv + c]);
                 o[c] = acc / l;
             }

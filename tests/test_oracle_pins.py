@@ -330,3 +330,54 @@ def test_attention_matches_high_precision_brute_force():
         for c in range(4):
             ref = mpmath.fsum(e[j] * mpmath.mpf(v[j, c]) for j in range(7)) / tot
             assert abs(float(ref) - O[0, i, c]) <= 1e-13 * (1.0 + abs(float(ref)))
+
+
+# ---- causal attention: query i attends keys 0..i only
+
+def test_causal_first_row_is_the_first_value_exactly():
+    Q, K, V = _attn_inputs(2, 6, 9, 16, 8, 600)
+    O, lse = oracle.attention_forward(Q, K, V, scale=0.25, with_lse=True, causal=True)
+    for b in range(2):
+        assert np.array_equal(O[b, 0], val(V[b])[0])                       # a softmax over one key is 1
+        dot = sum(Fraction(float(x)) * Fraction(float(y)) for x, y in zip(val(Q[b])[0], val(K[b])[0]))
+        assert lse[b, 0] == pytest.approx(float(Fraction(1, 4) * dot), rel=1e-15, abs=1e-15)
+
+
+def test_causal_rows_ignore_later_keys():
+    # Replacing keys and values after the diagonal leaves every earlier row unchanged.
+    Q, K, V = _attn_inputs(1, 12, 12, 16, 8, 610)
+    O = oracle.attention_forward(Q, K, V, causal=True)
+    for i in range(11):
+        K2, V2 = K.copy(), V.copy()
+        K2[0, i + 1:] = bf16(11 - i, 16, seed=620 + i)
+        V2[0, i + 1:] = bf16(11 - i, 8, seed=640 + i)
+        O2 = oracle.attention_forward(Q, K2, V2, causal=True)
+        assert np.array_equal(O2[0, :i + 1], O[0, :i + 1])
+        assert not np.array_equal(O2[0, i + 1:], O[0, i + 1:])
+
+
+def test_causal_last_rows_see_every_key():
+    # With more queries than keys, rows from sk - 1 on attend every key: the plain softmax.
+    Q, K, V = _attn_inputs(2, 10, 6, 16, 8, 650)
+    Oc, lc = oracle.attention_forward(Q, K, V, with_lse=True, causal=True)
+    O, l = oracle.attention_forward(Q, K, V, with_lse=True)
+    assert np.array_equal(Oc[:, 5:], O[:, 5:]) and np.array_equal(lc[:, 5:], l[:, 5:])
+    assert not np.allclose(Oc[:, :5], O[:, :5])
+
+
+def test_causal_matches_high_precision_brute_force():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    Q, K, V = _attn_inputs(1, 5, 4, 6, 3, 660)
+    scale = 0.47
+    O, lse = oracle.attention_forward(Q, K, V, scale=scale, with_lse=True, causal=True)
+    q, k, v = val(Q[0]), val(K[0]), val(V[0])
+    for i in range(5):
+        keys = range(min(i + 1, 4))
+        s = [mpmath.mpf(scale) * mpmath.fsum(mpmath.mpf(q[i, t]) * mpmath.mpf(k[j, t]) for t in range(6)) for j in keys]
+        e = [mpmath.exp(x) for x in s]
+        tot = mpmath.fsum(e)
+        assert abs(float(mpmath.log(tot)) - lse[0, i]) <= 1e-13
+        for c in range(3):
+            ref = mpmath.fsum(e[n] * mpmath.mpf(v[j, c]) for n, j in enumerate(keys)) / tot
+            assert abs(float(ref) - O[0, i, c]) <= 1e-13 * (1.0 + abs(float(ref)))
