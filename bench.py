@@ -540,7 +540,7 @@ def attn_oracle_sample(w: AttentionWorkload, budget_s: float, seed: int = 0):
     Returns (callable running the sample, TFLOP/s of one run, seconds, heads, threads).
     """
     import oracle
-    per_head = 4.0 * w.sq * w.sk * w.d
+    per_head = 4.0 * w.pairs * w.d
 
     def head_inputs(h):
         Q = inputs.bf16_matrix(h * w.sq, w.d, w.dist, seed + inputs.STREAM_A).reshape(h, w.sq, w.d)
@@ -550,14 +550,14 @@ def attn_oracle_sample(w: AttentionWorkload, budget_s: float, seed: int = 0):
 
     Q, K, V = head_inputs(1)
     t0 = time.perf_counter()
-    oracle.attention_forward(Q, K, V)
+    oracle.attention_forward(Q, K, V, causal=w.causal)
     rate = per_head / max(time.perf_counter() - t0, 1e-6)
     heads = max(1, min(w.batch, int(rate * budget_s / per_head)))
     Q, K, V = head_inputs(heads)
     t0 = time.perf_counter()
-    oracle.attention_forward(Q, K, V)
+    oracle.attention_forward(Q, K, V, causal=w.causal)
     secs = time.perf_counter() - t0
-    return (lambda: oracle.attention_forward(Q, K, V)), heads * per_head / secs / 1e12, secs, heads, \
+    return (lambda: oracle.attention_forward(Q, K, V, causal=w.causal)), heads * per_head / secs / 1e12, secs, heads, \
         oracle.num_threads()
 
 
@@ -577,14 +577,14 @@ def bench_attention_reference(args, w: AttentionWorkload):
         run()
         times.append(time.perf_counter() - t0)
     total = sum(times)
-    value = 4.0 * heads * w.sq * w.sk * w.d * args.steps / total / 1e12
+    value = 4.0 * heads * w.pairs * w.d * args.steps / total / 1e12
     sample = f"heads 0..{heads - 1} (all {w.sq} query rows against all {w.sk} keys) per step, of the " \
              f"{w.batch}-head workload"
     line = {
         "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "sq": w.sq, "sk": w.sk, "d": w.d,
+        "config": {"workload": w.name, "batch": w.batch, "sq": w.sq, "sk": w.sk, "d": w.d, "causal": w.causal,
                    "description": "fp64 CPU oracle (softmax of the fp64 scores, OpenMP over rows): " + w.description},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -618,7 +618,7 @@ def bench_attention_ours(args, w: AttentionWorkload):
     def run():
         nonlocal launches
         s = gemm.attention_forward_run(Q, K, V, O, lse, w.batch, w.sq, w.sk, w.d, 0.0, out_f32, cluster,
-                                       cta_group=cta_group, stream=stream)
+                                       cta_group=cta_group, causal=w.causal, stream=stream)
         if s != gemm.GEMM_OK:
             raise RuntimeError(f"attention_forward_run: status {s}")
         launches += 1
@@ -659,7 +659,7 @@ def bench_attention_ours(args, w: AttentionWorkload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "sq": w.sq, "sk": w.sk, "d": w.d, "out": w.out,
-                   "cluster": cluster, "cta_group": cta_group,
+                   "cluster": cluster, "cta_group": cta_group, "causal": w.causal,
                    "l2": f"no flush: the inputs ({input_bytes >> 20} MB) are larger than L2; the K steps "
                          f"run back to back between one pair of events",
                    "description": w.description},
@@ -706,7 +706,7 @@ def attn_e2e(w, args, device, stream, dist, cluster, cta_group, host_in):
 
     def step():
         s = gemm.attention_forward_run_host(Qp, Kp, Vp, O_h, lse_h, w.batch, w.sq, w.sk, w.d, ws, ws_bytes, 0.0,
-                                            out_f32, cluster, cta_group, stream)
+                                            out_f32, cluster, cta_group, causal=w.causal, stream=stream)
         if s != gemm.GEMM_OK:
             raise RuntimeError(f"attention_forward_run_host: status {s}")
 

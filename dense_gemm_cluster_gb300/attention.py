@@ -27,13 +27,13 @@ def measure(batch=128, sq=4096, sk=4096, d=128, cluster=2, steps=10, warmup=3, d
     lse = torch.empty(batch * sq, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
-        assert gemm.attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, 0.0, 0, cluster, cta_group, stream) == 0
+        assert gemm.attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, 0.0, 0, cluster, cta_group, stream=stream) == 0
     st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize(dev)
     for i in range(steps):
         st[i].record(stream)
-        gemm.attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, 0.0, 0, cluster, cta_group, stream)
+        gemm.attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, 0.0, 0, cluster, cta_group, stream=stream)
         en[i].record(stream)
     assert gemm.attention_forward_query_status(stream) == 0
     ms = sum(a.elapsed_time(b) for a, b in zip(st, en)) / steps

@@ -129,7 +129,7 @@ __device__ __forceinline__ uint32_t kmajor_koff_half(int k) {
 // MN-major tile (V: 128 keys x 128 d): K step of 16 keys = 16 rows of 128 bytes.
 __device__ __forceinline__ uint32_t mnmajor_koff(int k) { return (uint32_t)(k * 2048) >> 4; }
 
-template <bool PAIR>
+template <bool PAIR, bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -158,7 +158,18 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     // a whole cluster leaves together when the last z slice runs past the batch).
     const int b = (int)(blockIdx.z * gridDim.y + blockIdx.y);
     if (b >= p.batch) return;
-    const int q0 = blockIdx.x * (QT * TQ);
+    // Causal: query blocks run last-first (the longest rows start first), and a
+    // cluster, whose CTAs share every K/V tile, walks the key tiles its last query
+    // row needs; rows before the diagonal see the later keys masked.
+    const int bx0 = (int)(blockIdx.x - blockIdx.x % (unsigned)c);          // the cluster's first block
+    const int qblk = CAUSAL ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const int q0 = qblk * (QT * TQ);
+    int n_kv = p.n_kv;
+    if (CAUSAL) {
+        const long long last_q = min((long long)p.sq, (long long)((int)gridDim.x - bx0) * (QT * TQ)) - 1;
+        const long long keys = min((long long)p.sk, last_q + 1);
+        n_kv = (int)((keys + TK - 1) / TK);
+    }
 
     if (threadIdx.x == 0) {
         // Pair: the even CTA's q_full and kv_full count both CTAs' arms and bytes, its
@@ -198,7 +209,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         mbar_arrive_expect_tx_cluster(qb, QT * TILE_BYTES);
         for (int i = 0; i < QT; ++i)
             tma_load_4d_pair(smem_u32(sQ + i * TILE_BYTES), &tmQ, qb, 0, q0 + i * TQ, 0, b);
-        const int loads = 2 * p.n_kv;
+        const int loads = 2 * n_kv;
         for (int n = 0; n < loads; ++n) {
             const int s = n % NSL;
             const uint32_t ph = (uint32_t)(n / NSL) & 1u;
@@ -255,8 +266,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 return true;
             };
             if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
-            for (int j = 0; ok && j < p.n_kv; ++j) {
-                const bool more = j + 1 < p.n_kv;
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const bool more = j + 1 < n_kv;
                 ok = issue_pv(0, j) && (!more || issue_s(0, j + 1)) && issue_pv(1, j) && (!more || issue_s(1, j + 1));
             }
         }
@@ -276,7 +287,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         else { k_atom0 = (int)rank / (c / 2); k_r0 = ((int)rank % (c / 2)) * (TK / (c / 2)); }
         const int v_r0 = (int)rank * (TK / c);
         const uint32_t slice_bytes = TILE_BYTES / (uint32_t)c;
-        const int loads = 2 * p.n_kv;
+        const int loads = 2 * n_kv;
         for (int n = 0; n < loads; ++n) {
             const int s = n % NS;
             const uint32_t ph = (uint32_t)(n / NS) & 1u;
@@ -350,8 +361,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             return true;
         };
         if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
-        for (int j = 0; ok && j < p.n_kv; ++j) {
-            const bool more = j + 1 < p.n_kv;
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const bool more = j + 1 < n_kv;
             ok = issue_pv(0, j) && (!more || issue_s(0, j + 1)) && issue_pv(1, j) && (!more || issue_s(1, j + 1));
         }
     } else if (warp >= 4) {
@@ -366,12 +377,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         float m_ref = -INFINITY;                     // reference max, base-2 units
         float l = 0.0f;                              // running sum of 2^(x - m_ref)
         bool ok = true;
-        for (int j = 0; j < p.n_kv; ++j) {
+        const int q_row = q0 + ti * TQ + row;       // this thread's query
+        for (int j = 0; j < n_kv; ++j) {
             if (!attn_wait(smem_u32(&s_full[ti]), (uint32_t)j & 1u, p, 7)) { ok = false; break; }
             tc_fence_after();
             uint32_t x[TK];
             tmem_ld_128cols_wait(tS, x);
-            const int valid = p.sk - j * TK;         // keys of this tile inside the sequence
+            int valid = p.sk - j * TK;               // keys of this tile inside the sequence
+            if (CAUSAL) valid = min(valid, q_row - j * TK + 1);     // and not after this query
             if (valid < TK) {
 #pragma unroll
                 for (int i = 0; i < TK; ++i)
@@ -447,7 +460,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
         }
         // Final normalisation: O / l, and lse = (m_ref + log2 l) * ln 2.
-        if (ok && attn_wait(smem_u32(&pv_done[ti]), (uint32_t)(p.n_kv - 1) & 1u, p, 9)) {
+        if (ok && attn_wait(smem_u32(&pv_done[ti]), (uint32_t)(n_kv - 1) & 1u, p, 9)) {
             tc_fence_after();
             const int q = q0 + ti * TQ + row;
             const float inv = 1.0f / l;
@@ -518,7 +531,8 @@ bool encode(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* p
 
 extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, const void* V, void* O, float* lse,
                                                int64_t batch, int64_t sq, int64_t sk, int64_t d, float scale,
-                                               int out_f32, int cluster, int cta_group, void* stream) {
+                                               int out_f32, int cluster, int cta_group, int causal,
+                                               void* stream) {
     if (batch < 0 || sq < 0 || sk < 0) return afail(GEMM_ERR_INVALID_ARG, "negative size");
     if (batch == 0 || sq == 0) return GEMM_OK;
     if (sk == 0) return afail(GEMM_ERR_INVALID_ARG, "sk must be at least 1");
@@ -563,15 +577,17 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     p.out = O;
     p.lse = lse;
     p.timeout_ns = 2000000000ull;
-    void* fn = pair ? reinterpret_cast<void*>(&attention_fwd_kernel<true>)
-                    : reinterpret_cast<void*>(&attention_fwd_kernel<false>);
+    void* fn = pair ? (causal ? reinterpret_cast<void*>(&attention_fwd_kernel<true, true>)
+                              : reinterpret_cast<void*>(&attention_fwd_kernel<true, false>))
+                    : (causal ? reinterpret_cast<void*>(&attention_fwd_kernel<false, true>)
+                              : reinterpret_cast<void*>(&attention_fwd_kernel<false, false>));
     // Set the shared-memory limit once per device and kernel, so that a steady-state
     // call is one launch (and can be captured into a CUDA graph).
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));
-    static std::atomic<unsigned char> smem_set[64][2];
-    std::atomic<unsigned char>& flag = smem_set[dev & 63][pair ? 1 : 0];
+    static std::atomic<unsigned char> smem_set[64][4];
+    std::atomic<unsigned char>& flag = smem_set[dev & 63][(pair ? 1 : 0) + (causal ? 2 : 0)];
     if (!flag.load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));

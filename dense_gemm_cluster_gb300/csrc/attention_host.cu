@@ -77,8 +77,8 @@ extern "C" size_t attention_forward_host_workspace_bytes(int64_t batch, int64_t 
 
 extern "C" gemm_status_t attention_forward_run_host(const void* Q, const void* K, const void* V, void* O, float* lse,
                                                     int64_t batch, int64_t sq, int64_t sk, int64_t d, float scale,
-                                                    int out_f32, int cluster, int cta_group, void* workspace,
-                                                    size_t workspace_bytes, void* stream_v) {
+                                                    int out_f32, int cluster, int cta_group, int causal,
+                                                    void* workspace, size_t workspace_bytes, void* stream_v) {
     if (batch < 0 || sq < 0 || sk < 0) return GEMM_ERR_INVALID_ARG;
     if (batch == 0 || sq == 0) return GEMM_OK;
     if (sk == 0 || batch >= (1ll << 31) || sq >= (1ll << 31) || sk >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
@@ -128,7 +128,7 @@ extern "C" gemm_status_t attention_forward_run_host(const void* Q, const void* K
         if (e != cudaSuccess) break;
         s = attention_forward_run(ws + l.q + qo, ws + l.k + ko, ws + l.v + ko, ws + l.o + oo,
                                   lse ? reinterpret_cast<float*>(ws + l.lse + lo) : nullptr, hb, sq, sk, d, scale,
-                                  out_f32, cluster, cta_group, stream_v);
+                                  out_f32, cluster, cta_group, causal, stream_v);
         if (s != GEMM_OK) break;
         e = cudaEventRecord(pipe.ev_run[i], stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(pipe.out, pipe.ev_run[i], 0);

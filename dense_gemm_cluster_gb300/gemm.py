@@ -307,16 +307,17 @@ def stencil_1d_query_status(stream=None) -> int:
 
 
 # ---------------------------------------------------------------- fused attention forward (include/attention.h)
-_lib.attention_forward_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _i32, _i32, _vp]
+_lib.attention_forward_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _i32, _i32, _i32,
+                                       _vp]
 _lib.attention_forward_run.restype = _i32
 _lib.attention_forward_query_status.argtypes = [_vp]
 _lib.attention_forward_query_status.restype = _i32
 
 
 def attention_forward_run(Q, K, V, O, lse, batch, sq, sk, d, scale=0.0, out_f32=0, cluster=1, cta_group=1,
-                          stream=None) -> int:
+                          causal=0, stream=None) -> int:
     return _lib.attention_forward_run(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), batch, sq, sk, d, scale,
-                                      out_f32, cluster, cta_group, _stream(stream))
+                                      out_f32, cluster, cta_group, 1 if causal else 0, _stream(stream))
 
 
 def attention_forward_query_status(stream=None) -> int:
@@ -324,7 +325,7 @@ def attention_forward_query_status(stream=None) -> int:
 
 
 _lib.attention_forward_run_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _i32, _i32,
-                                            _i32, _vp, ctypes.c_size_t, _vp]
+                                            _i32, _i32, _vp, ctypes.c_size_t, _vp]
 _lib.attention_forward_run_host.restype = _i32
 _lib.attention_forward_host_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, _i32]
 _lib.attention_forward_host_workspace_bytes.restype = ctypes.c_size_t
@@ -335,8 +336,8 @@ def attention_forward_host_workspace_bytes(batch, sq, sk, d, out_f32=0) -> int:
 
 
 def attention_forward_run_host(Q, K, V, O, lse, batch, sq, sk, d, workspace, workspace_bytes, scale=0.0, out_f32=0,
-                               cluster=1, cta_group=1, stream=None) -> int:
+                               cluster=1, cta_group=1, causal=0, stream=None) -> int:
     """Host Q, K, V, O, lse (numpy arrays or pinned CPU tensors); `workspace` is device memory."""
     return _lib.attention_forward_run_host(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), batch, sq, sk, d, scale,
-                                           out_f32, cluster, cta_group, _ptr(workspace), workspace_bytes,
-                                           _stream(stream))
+                                           out_f32, cluster, cta_group, 1 if causal else 0, _ptr(workspace),
+                                           workspace_bytes, _stream(stream))

@@ -101,11 +101,21 @@ class AttentionWorkload:
     cta_group: int = 1              # 1: multicast of whole K/V tiles; 2: pair MMA over half tiles
     out: str = "bf16"
     dist: str = "normal"
+    causal: bool = False            # query i attends keys 0..i only
     description: str = ""
 
     @property
+    def pairs(self) -> int:
+        """(query, key) pairs scored per head."""
+        if not self.causal:
+            return self.sq * self.sk
+        full = max(0, self.sq - self.sk)                          # rows past the last key see every key
+        n = min(self.sq, self.sk)
+        return n * (n + 1) // 2 + full * self.sk
+
+    @property
     def flops(self) -> int:
-        return 4 * self.batch * self.sq * self.sk * self.d        # Q K^T and P V
+        return 4 * self.batch * self.pairs * self.d               # Q K^T and P V over the scored pairs
 
     def min_hbm_bytes(self) -> int:
         """Q, K, V read once; O and the row log-sum-exp written once."""
@@ -119,4 +129,8 @@ ATTENTION_WORKLOADS = {
         description="fused attention forward O = softmax(Q K^T / sqrt(128)) V with the row log-sum-exp, "
                     "batch 8 x heads 16, seq 4096, head dim 128, N(0,1) bf16 Q/K/V, bf16 O, each K/V tile "
                     "multicast across the 2 query-block CTAs of a cluster"),
+    "attention_fwd_causal_8x16x4096x4096x128": AttentionWorkload(
+        "attention_fwd_causal_8x16x4096x4096x128", 128, 4096, 4096, cluster=2, causal=True,
+        description="the attention forward above with the causal mask (query i attends keys 0..i): half the "
+                    "score pairs, FLOPs counted over the pairs scored"),
 }

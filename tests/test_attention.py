@@ -24,7 +24,7 @@ def _inputs(b, sq, sk, seed, k_growth=0.0):
     return Q, K, V
 
 
-def _run(Q, K, V, cluster, out_f32=0, scale=0.0, cta_group=1):
+def _run(Q, K, V, cluster, out_f32=0, scale=0.0, cta_group=1, causal=False):
     import torch
     from dense_gemm_cluster_gb300 import gemm
     b, sq, _ = Q.shape
@@ -32,7 +32,8 @@ def _run(Q, K, V, cluster, out_f32=0, scale=0.0, cta_group=1):
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
     O = torch.full((b * sq * 128,), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
     lse = torch.full((b * sq,), float("nan"), dtype=torch.float32, device="cuda")
-    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, 128, scale, out_f32, cluster, cta_group)
+    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, 128, scale, out_f32, cluster, cta_group,
+                                   causal=causal)
     assert s == gemm.GEMM_OK
     assert gemm.attention_forward_query_status() == gemm.GEMM_OK
     o = O.float().cpu().numpy().reshape(b, sq, 128).astype(np.float64)
@@ -212,3 +213,28 @@ def test_attention_more_heads_than_one_grid_dimension_holds():
     vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V[heads]))))
     assert np.max(np.abs(o[heads] - ref)) <= 1e-2 * vmax
     assert np.max(np.abs(l[heads] - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+
+
+@pytest.mark.parametrize("b,sq,sk", [(2, 256, 256), (1, 300, 500), (1, 700, 300), (3, 1000, 1000), (1, 129, 1),
+                                    (2, 1300, 1300)])
+@pytest.mark.parametrize("cluster,cta_group", MODES)
+def test_causal_attention_matches_oracle(b, sq, sk, cluster, cta_group):
+    # Query i attends keys 0..i: diagonal tiles are masked row by row, a cluster stops at
+    # the key tiles its last query needs, and query blocks run last-first.
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    Q, K, V = _inputs(b, sq, sk, 700 + sq)
+    o, lse = _run(Q, K, V, cluster, out_f32=1, cta_group=cta_group, causal=True)
+    ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True, causal=True)
+    vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+    assert np.isfinite(o).all()
+    assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
+    assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+
+
+def test_causal_sharing_modes_are_bit_identical():
+    Q, K, V = _inputs(2, 900, 900, 19)
+    base, base_lse = _run(Q, K, V, 1, out_f32=1, causal=True)
+    for c, g in MODES[1:]:
+        o, lse = _run(Q, K, V, c, out_f32=1, cta_group=g, causal=True)
+        assert np.array_equal(o, base) and np.array_equal(lse, base_lse), (c, g)
