@@ -154,19 +154,29 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int c = p.cluster;
     const uint32_t rank = c > 1 ? cluster_ctarank() : 0u;
     const uint16_t all = (uint16_t)((1u << c) - 1u);
-    // Heads: grid y, continued in grid z past 65535 (a cluster spans grid x only, so
-    // a whole cluster leaves together when the last z slice runs past the batch).
-    const int b = (int)(blockIdx.z * gridDim.y + blockIdx.y);
+    // Not causal: grid x = query blocks, heads in grid y, continued in grid z past
+    // 65535. Causal: grid x = heads x the c blocks of a cluster, grid y = groups of c
+    // query blocks, last group first, so every head's longest rows start before any
+    // shorter ones. A cluster spans grid x within one head either way, so it leaves
+    // together when the grid runs past the batch.
+    int b, qblk, cluster_last_qblk;
+    if (CAUSAL) {
+        b = (int)(blockIdx.x / (unsigned)c + blockIdx.z * (gridDim.x / (unsigned)c));
+        const int group = (int)gridDim.y - 1 - (int)blockIdx.y;
+        qblk = group * c + (int)(blockIdx.x % (unsigned)c);
+        cluster_last_qblk = group * c + c - 1;
+    } else {
+        b = (int)(blockIdx.z * gridDim.y + blockIdx.y);
+        qblk = (int)blockIdx.x;
+        cluster_last_qblk = qblk;
+    }
     if (b >= p.batch) return;
-    // Causal: query blocks run last-first (the longest rows start first), and a
-    // cluster, whose CTAs share every K/V tile, walks the key tiles its last query
-    // row needs; rows before the diagonal see the later keys masked.
-    const int bx0 = (int)(blockIdx.x - blockIdx.x % (unsigned)c);          // the cluster's first block
-    const int qblk = CAUSAL ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
     const int q0 = qblk * (QT * TQ);
     int n_kv = p.n_kv;
     if (CAUSAL) {
-        const long long last_q = min((long long)p.sq, (long long)((int)gridDim.x - bx0) * (QT * TQ)) - 1;
+        // A cluster's CTAs share every K/V tile: walk the key tiles its last query needs;
+        // rows before the diagonal see the later keys masked.
+        const long long last_q = min((long long)p.sq, (long long)(cluster_last_qblk + 1) * (QT * TQ)) - 1;
         const long long keys = min((long long)p.sk, last_q + 1);
         n_kv = (int)((keys + TK - 1) / TK);
     }
@@ -602,8 +612,15 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     attr[0].val.clusterDim.x = cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    const unsigned gy = (unsigned)(batch < 65535 ? batch : 65535);
-    cfg.gridDim = dim3((unsigned)ctas, gy, (unsigned)((batch + gy - 1) / gy));
+    if (causal && ctas / cluster > 65535)
+        return afail(GEMM_ERR_UNSUPPORTED, "causal: at most 65535 groups of query blocks (sq up to 65535 * 256 * cluster)");
+    if (causal) {
+        const long long hx = batch < (1ll << 30) / cluster ? batch : (1ll << 30) / cluster;
+        cfg.gridDim = dim3((unsigned)(hx * cluster), (unsigned)(ctas / cluster), (unsigned)((batch + hx - 1) / hx));
+    } else {
+        const unsigned gy = (unsigned)(batch < 65535 ? batch : 65535);
+        cfg.gridDim = dim3((unsigned)ctas, gy, (unsigned)((batch + gy - 1) / gy));
+    }
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = static_cast<cudaStream_t>(stream);
