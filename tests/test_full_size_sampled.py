@@ -87,14 +87,16 @@ def test_scores_workload_full_size_sampled():
         assert 0.8 < float(S.std()) / math.sqrt(w.K) < 1.25
 
 
-def test_attention_workload_full_size_sampled():
+@pytest.mark.parametrize("name", ["attention_fwd_8x16x4096x4096x128", "attention_fwd_causal_8x16x4096x4096x128"])
+def test_attention_workload_full_size_sampled(name):
     # The bench's attention launch (all 128 heads, its cluster size); rows of six heads
-    # are checked against the oracle, which treats each query row independently.
+    # are checked against the oracle, which treats each query row independently (a causal
+    # row r is the plain softmax over keys 0..r).
     import torch
     import oracle
     from dense_gemm_cluster_gb300 import gemm, inputs
     from dense_gemm_cluster_gb300.workloads import ATTENTION_WORKLOADS
-    w = ATTENTION_WORKLOADS["attention_fwd_8x16x4096x4096x128"]
+    w = ATTENTION_WORKLOADS[name]
     Q = inputs.bf16_matrix(w.batch * w.sq, w.d, w.dist, inputs.STREAM_A).reshape(w.batch, w.sq, w.d)
     K = inputs.bf16_matrix(w.batch * w.sk, w.d, w.dist, inputs.STREAM_B).reshape(w.batch, w.sk, w.d)
     V = inputs.bf16_matrix(w.batch * w.sk, w.d, w.dist, inputs.STREAM_C).reshape(w.batch, w.sk, w.d)
@@ -102,7 +104,7 @@ def test_attention_workload_full_size_sampled():
     O = torch.empty(w.batch * w.sq * w.d, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(w.batch * w.sq, dtype=torch.float32, device="cuda")
     s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, w.batch, w.sq, w.sk, w.d, 0.0, 0, w.cluster,
-                                   w.cta_group)
+                                   w.cta_group, causal=w.causal)
     assert s == gemm.GEMM_OK and gemm.attention_forward_query_status() == gemm.GEMM_OK
     O = O.view(w.batch, w.sq, w.d)
     lse = lse.view(w.batch, w.sq)
@@ -111,7 +113,13 @@ def test_attention_workload_full_size_sampled():
     vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
     for b in sorted(set([0, w.batch - 1] + list(rng.integers(0, w.batch, size=4)))):
         rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, w.sq - 1], rng.integers(0, w.sq, size=26)]))
-        ref, ref_lse = oracle.attention_forward(Q[b:b + 1, rows], K[b:b + 1], V[b:b + 1], with_lse=True)
+        if w.causal:
+            parts = [oracle.attention_forward(Q[b:b + 1, [r]], K[b:b + 1, :r + 1], V[b:b + 1, :r + 1], with_lse=True)
+                     for r in rows]
+            ref = np.concatenate([o for o, _ in parts], axis=1)
+            ref_lse = np.concatenate([l for _, l in parts], axis=1)
+        else:
+            ref, ref_lse = oracle.attention_forward(Q[b:b + 1, rows], K[b:b + 1], V[b:b + 1], with_lse=True)
         got = O[b, torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
         got_lse = lse[b, torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
         assert np.max(np.abs(got - ref[0])) <= 1e-2 * vmax, f"head {b}"
