@@ -218,13 +218,14 @@ def test_attention_more_heads_than_one_grid_dimension_holds():
 @pytest.mark.parametrize("b,sq,sk", [(2, 256, 256), (1, 300, 500), (1, 700, 300), (3, 1000, 1000), (1, 129, 1),
                                     (2, 1300, 1300)])
 @pytest.mark.parametrize("cluster,cta_group", MODES)
-def test_causal_attention_matches_oracle(b, sq, sk, cluster, cta_group):
+@pytest.mark.parametrize("out_f32", [0, 1])
+def test_causal_attention_matches_oracle(b, sq, sk, cluster, cta_group, out_f32):
     # Query i attends keys 0..i: diagonal tiles are masked row by row, a cluster stops at
     # the key tiles its last query needs, and query blocks run last-first.
     import oracle
     from dense_gemm_cluster_gb300 import inputs
     Q, K, V = _inputs(b, sq, sk, 700 + sq)
-    o, lse = _run(Q, K, V, cluster, out_f32=1, cta_group=cta_group, causal=True)
+    o, lse = _run(Q, K, V, cluster, out_f32=out_f32, cta_group=cta_group, causal=True)
     ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True, causal=True)
     vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
     assert np.isfinite(o).all()
