@@ -43,18 +43,36 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles the library if it is missing or older than its sources; returns its path."""
+    """Compiles the library if it is missing or older than its sources; returns its path.
+
+    Each translation unit compiles in its own nvcc process (in parallel), then one
+    nvcc call links the shared library."""
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I", INCLUDE, *SOURCES, "-o", tmp]
+    tag = f"{os.getpid()}"
+    flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+        flags.insert(0, "-Xptxas=-v")
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(BUILD_DIR, os.path.basename(src) + f".{tag}.o")
+        cmd = [nvcc(), *flags, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        procs.append((subprocess.Popen(cmd), cmd))
+        objs.append(obj)
+    failed = [cmd for proc, cmd in procs if proc.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = LIB_PATH + f".{tag}.tmp"
+        subprocess.run([nvcc(), *ARCH, "-shared", *objs, "-o", tmp], check=True)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB_PATH
 
 
