@@ -26,11 +26,17 @@
  *
  * Work is spread by a persistent, cluster-launched kernel that walks output
  * tiles with a static stride ("Clusters, distributed shared memory & cluster
- * launch control", sections "Thread-block clusters" and "The second wall").
+ * launch control", sections "Thread-block clusters" and "The second wall"),
+ * splitting the last waves' k-blocks across clusters (stream-K) or, on request,
+ * taking tiles by cluster launch control. Launches carry the programmatic
+ * stream serialization attribute: a GEMM may start its prologue while the
+ * previous kernel in the stream drains, and waits for it to complete before
+ * touching global memory.
  *
  * Conventions for every call:
  *   - Pointers A, B, C are DEVICE pointers owned by the caller (except in
- *     gemm_run_host, where they are host pointers). The library never frees them.
+ *     gemm_run_host and gemm_run_strided_batched_host, where they are host
+ *     pointers). The library never frees them.
  *   - Sizes and leading dimensions are in elements. A row-major X has its last
  *     index contiguous: element (r, c) at X[r*ld + c]; column-major: X[c*ld + r].
  *   - stream is a cudaStream_t passed as void* (NULL = the legacy default stream).
