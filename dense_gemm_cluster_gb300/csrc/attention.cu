@@ -180,6 +180,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         const long long keys = min((long long)p.sk, last_q + 1);
         n_kv = (int)((keys + TK - 1) / TK);
     }
+    // Key tiles each query tile of this CTA scores: the cluster's count, or (causal,
+    // single-CTA MMAs) only those up to the tile's last query. Past its count a tile
+    // issues no MMA, but the last tile still releases every K/V slot.
+    auto n_kv_tile = [&](int i) -> int {
+        if (!CAUSAL || PAIR) return n_kv;
+        const long long keys = min((long long)p.sk, (long long)q0 + (i + 1) * TQ);
+        return max(1, min(n_kv, (int)((keys + TK - 1) / TK)));
+    };
 
     if (threadIdx.x == 0) {
         // Pair: the even CTA's q_full and kv_full count both CTAs' arms and bytes, its
@@ -340,12 +348,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 if (!attn_wait(smem_u32(&kv_full[s]), (uint32_t)(n / NS) & 1u, p, 3)) return false;
                 tc_fence_after();
             }
-            const uint64_t dq = smem_desc_sw128(smem_u32(sQ + i * TILE_BYTES), false, 0);
-            const uint64_t dk = ring_k + ((s * TILE_BYTES) >> 4);
+            if (j < n_kv_tile(i)) {
+                const uint64_t dq = smem_desc_sw128(smem_u32(sQ + i * TILE_BYTES), false, 0);
+                const uint64_t dk = ring_k + ((s * TILE_BYTES) >> 4);
 #pragma unroll
-            for (int k = 0; k < HD / 16; ++k)
-                mma_bf16<1>(tmem + i * TK, dq + kmajor_koff(k), dk + kmajor_koff(k), idesc_s, k > 0 ? 1u : 0u);
-            mma_commit<1>(smem_u32(&s_full[i]));
+                for (int k = 0; k < HD / 16; ++k)
+                    mma_bf16<1>(tmem + i * TK, dq + kmajor_koff(k), dk + kmajor_koff(k), idesc_s, k > 0 ? 1u : 0u);
+                mma_commit<1>(smem_u32(&s_full[i]));
+            }
             if (i == QT - 1) {
                 if (c > 1) mma_commit_mcast<1>(smem_u32(&kv_empty[s]), all);
                 else       mma_commit<1>(smem_u32(&kv_empty[s]));
@@ -356,14 +366,16 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         auto issue_pv = [&](int i, int j) -> bool {
             const int n = 2 * j + 1, s = n % NS;
             if (i == 0 && !attn_wait(smem_u32(&kv_full[s]), (uint32_t)(n / NS) & 1u, p, 4)) return false;
-            if (!attn_wait(smem_u32(&p_full[i]), (uint32_t)j & 1u, p, 5)) return false;
-            tc_fence_after();
-            const uint64_t dv = ring_v + ((s * TILE_BYTES) >> 4);
+            if (j < n_kv_tile(i)) {
+                if (!attn_wait(smem_u32(&p_full[i]), (uint32_t)j & 1u, p, 5)) return false;
+                tc_fence_after();
+                const uint64_t dv = ring_v + ((s * TILE_BYTES) >> 4);
 #pragma unroll
-            for (int k = 0; k < TK / 16; ++k)
-                mma_bf16_ts(tmem + 2 * TK + i * HD, tmem + i * TK + k * 8, dv + mnmajor_koff(k), idesc_o,
-                            (j > 0 || k > 0) ? 1u : 0u);
-            mma_commit<1>(smem_u32(&pv_done[i]));
+                for (int k = 0; k < TK / 16; ++k)
+                    mma_bf16_ts(tmem + 2 * TK + i * HD, tmem + i * TK + k * 8, dv + mnmajor_koff(k), idesc_o,
+                                (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit<1>(smem_u32(&pv_done[i]));
+            }
             if (i == QT - 1) {
                 if (c > 1) mma_commit_mcast<1>(smem_u32(&kv_empty[s]), all);
                 else       mma_commit<1>(smem_u32(&kv_empty[s]));
@@ -388,7 +400,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         float l = 0.0f;                              // running sum of 2^(x - m_ref)
         bool ok = true;
         const int q_row = q0 + ti * TQ + row;       // this thread's query
-        for (int j = 0; j < n_kv; ++j) {
+        const int n_kv_mine = n_kv_tile(ti);
+        for (int j = 0; j < n_kv_mine; ++j) {
             if (!attn_wait(smem_u32(&s_full[ti]), (uint32_t)j & 1u, p, 7)) { ok = false; break; }
             tc_fence_after();
             uint32_t x[TK];
@@ -470,7 +483,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
         }
         // Final normalisation: O / l, and lse = (m_ref + log2 l) * ln 2.
-        if (ok && attn_wait(smem_u32(&pv_done[ti]), (uint32_t)(n_kv - 1) & 1u, p, 9)) {
+        if (ok && attn_wait(smem_u32(&pv_done[ti]), (uint32_t)(n_kv_mine - 1) & 1u, p, 9)) {
             tc_fence_after();
             const int q = q0 + ti * TQ + row;
             const float inv = 1.0f / l;
