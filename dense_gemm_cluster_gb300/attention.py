@@ -1,6 +1,6 @@
 """Throughput of the fused attention forward (include/attention.h).
 
-    python -m dense_gemm_cluster_gb300.attention [--batch B] [--sq S] [--sk S] [--cluster C]
+    python -m dense_gemm_cluster_gb300.attention [--batch B] [--sq S] [--sk S] [--d D] [--cluster C]
                                                  [--cta-group G] [--causal] [--steps K] [--warmup W]
 
 One JSON line per cluster size: TFLOP/s (4 * batch * d per scored (query, key)
@@ -60,6 +60,7 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=128)
     ap.add_argument("--sq", type=int, default=4096)
     ap.add_argument("--sk", type=int, default=4096)
+    ap.add_argument("--d", type=int, choices=(64, 128), default=128, help="head dimension")
     ap.add_argument("--cluster", type=int, choices=(1, 2, 4), default=None, help="one cluster size (default: all)")
     ap.add_argument("--cta-group", type=int, choices=(1, 2), default=1, help="2: pair MMA (cluster 2)")
     ap.add_argument("--causal", action="store_true", help="query i attends keys 0..i only")
@@ -67,8 +68,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args(argv)
     configs = [(args.cluster, args.cta_group)] if args.cluster else [(1, 1), (2, 1), (4, 1), (2, 2)]
+    if args.d != 128:
+        configs = [(c, g) for c, g in configs if g == 1]
     for c, g in configs:
-        print(json.dumps(measure(args.batch, args.sq, args.sk, 128, c, args.steps, args.warmup, cta_group=g,
+        print(json.dumps(measure(args.batch, args.sq, args.sk, args.d, c, args.steps, args.warmup, cta_group=g,
                                  causal=args.causal)), flush=True)
     return 0
 

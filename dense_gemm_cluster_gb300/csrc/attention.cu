@@ -53,13 +53,13 @@ using namespace dgc;
 constexpr int TQ = 128;                  // queries per tile
 constexpr int QT = 2;                    // query tiles per CTA
 constexpr int TK = 128;                  // keys per tile
-constexpr int HD = 128;                  // head dimension
 constexpr int THREADS = 384;
-constexpr uint32_t TILE_BYTES = 128 * HD * 2;   // 32 KB: a Q, K or V tile
 constexpr uint32_t ATOM_BYTES = 128 * 128;      // one 64-element swizzle atom of a 128-row tile
 constexpr int NS = 4;                           // ring slots; K and V tiles alternate
 constexpr float RESCALE_THRESHOLD = 8.0f;       // log2 units: move the reference max past 2^8 growth
-constexpr size_t SMEM_BYTES = 1024 + (QT + NS) * TILE_BYTES + 24 * 8 + 16;
+// A Q, K or V tile is 128 rows of the head dimension (32 KB at 128, 16 KB at 64).
+__host__ __device__ constexpr uint32_t tile_bytes(int hd) { return 128u * (uint32_t)hd * 2u; }
+constexpr size_t smem_bytes(int hd) { return 1024 + (QT + NS) * (size_t)tile_bytes(hd) + 24 * 8 + 16; }
 
 __device__ unsigned int g_attn_status[4];
 
@@ -129,12 +129,16 @@ __device__ __forceinline__ uint32_t kmajor_koff_half(int k) {
 // MN-major tile (V: 128 keys x 128 d): K step of 16 keys = 16 rows of 128 bytes.
 __device__ __forceinline__ uint32_t mnmajor_koff(int k) { return (uint32_t)(k * 2048) >> 4; }
 
-template <bool PAIR, bool CAUSAL>
+template <bool PAIR, bool CAUSAL, int HD>
 __global__ void __launch_bounds__(THREADS, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     // Ring: NS slots of a whole K or V tile, or (pair) twice as many of half tiles.
     constexpr int NSL = PAIR ? 2 * NS : NS;
+    static_assert(HD == 64 || HD == 128, "head dimension 64 or 128");
+    static_assert(!PAIR || HD == 128, "the pair MMA splits 128 head columns");
+    constexpr uint32_t TILE_BYTES = tile_bytes(HD);
+    constexpr int ATOMS = HD / 64;                    // 128-byte swizzle atoms across a Q or K row
     constexpr uint32_t SLOT_BYTES = PAIR ? TILE_BYTES / 2 : TILE_BYTES;
     constexpr int G = PAIR ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
@@ -297,12 +301,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         mbar_arrive_expect_tx_local(smem_u32(q_full), QT * TILE_BYTES);
         for (int i = 0; i < QT; ++i)
             tma_load_4d(smem_u32(sQ + i * TILE_BYTES), &tmQ, smem_u32(q_full), 0, q0 + i * TQ, 0, b);
-        // This CTA's slice of each shared tile. K (K-major, 2 atoms): whole atoms
-        // first, then rows within an atom. V (MN-major, 2 boxes of 64 d columns x 128
-        // keys): a band of key rows of both boxes.
+        // This CTA's slice of each shared tile. K (K-major, HD / 64 atoms): whole atoms
+        // first, then rows within an atom. V (MN-major, HD / 64 boxes of 64 d columns x
+        // 128 keys): a band of key rows of every box.
         int k_atom0 = 0, k_r0 = 0;
-        if (c <= 2) { k_atom0 = (int)rank; }
-        else { k_atom0 = (int)rank / (c / 2); k_r0 = ((int)rank % (c / 2)) * (TK / (c / 2)); }
+        if (c <= ATOMS) { k_atom0 = (int)rank * (ATOMS / c); }
+        else { k_atom0 = (int)rank / (c / ATOMS); k_r0 = ((int)rank % (c / ATOMS)) * (TK / (c / ATOMS)); }
         const int v_r0 = (int)rank * (TK / c);
         const uint32_t slice_bytes = TILE_BYTES / (uint32_t)c;
         const int loads = 2 * n_kv;
@@ -559,10 +563,11 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     if (batch < 0 || sq < 0 || sk < 0) return afail(GEMM_ERR_INVALID_ARG, "negative size");
     if (batch == 0 || sq == 0) return GEMM_OK;
     if (sk == 0) return afail(GEMM_ERR_INVALID_ARG, "sk must be at least 1");
-    if (d != HD) return afail(GEMM_ERR_UNSUPPORTED, "head dimension must be 128");
+    if (d != 64 && d != 128) return afail(GEMM_ERR_UNSUPPORTED, "head dimension must be 64 or 128");
     if (cluster != 1 && cluster != 2 && cluster != 4) return afail(GEMM_ERR_UNSUPPORTED, "cluster must be 1, 2 or 4");
     if (cta_group != 1 && cta_group != 2) return afail(GEMM_ERR_UNSUPPORTED, "cta_group must be 1 or 2");
     if (cta_group == 2 && cluster != 2) return afail(GEMM_ERR_UNSUPPORTED, "the pair MMA runs in clusters of 2");
+    if (cta_group == 2 && d != 128) return afail(GEMM_ERR_UNSUPPORTED, "the pair MMA needs head dimension 128");
     const bool pair = cta_group == 2;
     if (!Q || !K || !V || !O) return afail(GEMM_ERR_INVALID_ARG, "null pointer");
     if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
@@ -572,19 +577,22 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     auto enc = attn_encoder();
     if (!enc) return afail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     CUtensorMap tq, tk, tv;
-    // Q and K: the k-split view {64, rows, 2 atoms, batch} (atoms 128 bytes apart).
-    const cuuint64_t qd[4] = {64, (cuuint64_t)sq, 2, (cuuint64_t)batch};
-    const cuuint64_t qs[3] = {HD * 2, 128, (cuuint64_t)(sq * HD * 2)};
-    const cuuint32_t qb[4] = {64, TQ, 2, 1};
-    const cuuint64_t kd[4] = {64, (cuuint64_t)sk, 2, (cuuint64_t)batch};
-    const cuuint64_t ks[3] = {HD * 2, 128, (cuuint64_t)(sk * HD * 2)};
-    // A K slice: whole atoms first (cluster <= 2), then half the rows of one atom (cluster 4);
-    // pair mode: half the keys, both atoms.
-    const cuuint32_t kb[4] = {64, (cuuint32_t)(pair ? TK / 2 : (cluster <= 2 ? TK : TK / 2)),
-                              (cuuint32_t)(pair || cluster == 1 ? 2 : 1), 1};
+    const int64_t HD = d;
+    const int atoms = (int)(d / 64);                      // 128-byte swizzle atoms across a row
+    // Q and K: the k-split view {64, rows, atoms, batch} (atoms 128 bytes apart).
+    const cuuint64_t qd[4] = {64, (cuuint64_t)sq, (cuuint64_t)atoms, (cuuint64_t)batch};
+    const cuuint64_t qs[3] = {(cuuint64_t)(HD * 2), 128, (cuuint64_t)(sq * HD * 2)};
+    const cuuint32_t qb[4] = {64, TQ, (cuuint32_t)atoms, 1};
+    const cuuint64_t kd[4] = {64, (cuuint64_t)sk, (cuuint64_t)atoms, (cuuint64_t)batch};
+    const cuuint64_t ks[3] = {(cuuint64_t)(HD * 2), 128, (cuuint64_t)(sk * HD * 2)};
+    // A K slice: whole atoms first, then bands of rows within an atom; pair mode: half
+    // the keys, every atom.
+    const int k_rows = pair ? TK / 2 : (cluster <= atoms ? TK : TK / (cluster / atoms));
+    const int k_atoms = pair ? atoms : (cluster <= atoms ? atoms / cluster : 1);
+    const cuuint32_t kb[4] = {64, (cuuint32_t)k_rows, (cuuint32_t)k_atoms, 1};
     // V: MN-major boxes of 64 d columns x (128 / cluster) keys (pair mode: all 128 keys).
-    const cuuint64_t vd[3] = {HD, (cuuint64_t)sk, (cuuint64_t)batch};
-    const cuuint64_t vs[2] = {HD * 2, (cuuint64_t)(sk * HD * 2)};
+    const cuuint64_t vd[3] = {(cuuint64_t)HD, (cuuint64_t)sk, (cuuint64_t)batch};
+    const cuuint64_t vs[2] = {(cuuint64_t)(HD * 2), (cuuint64_t)(sk * HD * 2)};
     const cuuint32_t vb[3] = {64, (cuuint32_t)(pair ? TK : TK / cluster), 1};
     if (!encode(enc, &tq, Q, 4, qd, qs, qb) || !encode(enc, &tk, K, 4, kd, ks, kb) || !encode(enc, &tv, V, 3, vd, vs, vb))
         return afail(GEMM_ERR_INVALID_ARG, "tensor map encode failed");
@@ -600,19 +608,23 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     p.out = O;
     p.lse = lse;
     p.timeout_ns = 2000000000ull;
-    void* fn = pair ? (causal ? reinterpret_cast<void*>(&attention_fwd_kernel<true, true>)
-                              : reinterpret_cast<void*>(&attention_fwd_kernel<true, false>))
-                    : (causal ? reinterpret_cast<void*>(&attention_fwd_kernel<false, true>)
-                              : reinterpret_cast<void*>(&attention_fwd_kernel<false, false>));
+    void* fn;
+    if (pair) fn = causal ? reinterpret_cast<void*>(&attention_fwd_kernel<true, true, 128>)
+                          : reinterpret_cast<void*>(&attention_fwd_kernel<true, false, 128>);
+    else if (d == 128) fn = causal ? reinterpret_cast<void*>(&attention_fwd_kernel<false, true, 128>)
+                                   : reinterpret_cast<void*>(&attention_fwd_kernel<false, false, 128>);
+    else fn = causal ? reinterpret_cast<void*>(&attention_fwd_kernel<false, true, 64>)
+                     : reinterpret_cast<void*>(&attention_fwd_kernel<false, false, 64>);
+    const size_t smem = smem_bytes((int)d);
     // Set the shared-memory limit once per device and kernel, so that a steady-state
     // call is one launch (and can be captured into a CUDA graph).
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));
-    static std::atomic<unsigned char> smem_set[64][4];
-    std::atomic<unsigned char>& flag = smem_set[dev & 63][(pair ? 1 : 0) + (causal ? 2 : 0)];
+    static std::atomic<unsigned char> smem_set[64][8];
+    std::atomic<unsigned char>& flag = smem_set[dev & 63][(pair ? 1 : 0) + (causal ? 2 : 0) + (d == 64 ? 4 : 0)];
     if (!flag.load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return afail(GEMM_ERR_CUDA, cudaGetErrorString(e));
         flag.store(1, std::memory_order_release);
     }
@@ -635,7 +647,7 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
         cfg.gridDim = dim3((unsigned)ctas, gy, (unsigned)((batch + gy - 1) / gy));
     }
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cfg.attrs = attr;
     cfg.numAttrs = 1;

@@ -82,8 +82,8 @@ extern "C" gemm_status_t attention_forward_run_host(const void* Q, const void* K
     if (batch < 0 || sq < 0 || sk < 0) return GEMM_ERR_INVALID_ARG;
     if (batch == 0 || sq == 0) return GEMM_OK;
     if (sk == 0 || batch >= (1ll << 31) || sq >= (1ll << 31) || sk >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
-    if (d != 128 || (cluster != 1 && cluster != 2 && cluster != 4) || (cta_group != 1 && cta_group != 2) ||
-        (cta_group == 2 && cluster != 2))
+    if ((d != 64 && d != 128) || (cluster != 1 && cluster != 2 && cluster != 4) || (cta_group != 1 && cta_group != 2) ||
+        (cta_group == 2 && (cluster != 2 || d != 128)))
         return GEMM_ERR_UNSUPPORTED;
     if (!Q || !K || !V || !O || !workspace) return GEMM_ERR_INVALID_ARG;
     const Layout l = layout_for(batch, sq, sk, d, out_f32);

@@ -175,7 +175,8 @@ def test_attention_validation_before_launch(lib):
     # addresses are never dereferenced.
     a, m = 1 << 20, (1 << 20) + 2                # 16-byte aligned / misaligned fake addresses
     run = lib.attention_forward_run
-    assert run(a, a, a, a, None, 1, 128, 128, 64) == lib.GEMM_ERR_UNSUPPORTED          # head dim
+    assert run(a, a, a, a, None, 1, 128, 128, 96) == lib.GEMM_ERR_UNSUPPORTED          # head dim
+    assert run(a, a, a, a, None, 1, 128, 128, 64, 0.0, 0, 2, 2) == lib.GEMM_ERR_UNSUPPORTED   # pair needs 128
     assert run(a, a, a, a, None, 1, 128, 128, 128, 0.0, 0, 3) == lib.GEMM_ERR_UNSUPPORTED
     assert run(a, a, a, a, None, 1, 128, 128, 128, 0.0, 0, 4, 2) == lib.GEMM_ERR_UNSUPPORTED         # pair needs 2
     assert run(a, a, a, a, None, 1, 128, 128, 128, 0.0, 0, 2, 3) == lib.GEMM_ERR_UNSUPPORTED
@@ -195,6 +196,7 @@ def test_attention_validation_before_launch(lib):
     assert host(a, a, a, a, None, 2, 300, 500, 128, a, need - 1) == lib.GEMM_ERR_INVALID_ARG     # short
     assert host(a, a, a, a, None, 2, 300, 500, 128, None, need) == lib.GEMM_ERR_INVALID_ARG      # missing
     assert host(a, a, a, a, None, 2, 300, 500, 128, a + 16, need) == lib.GEMM_ERR_ALIGNMENT     # not 256-B aligned
-    assert host(a, a, a, a, None, 2, 300, 500, 64, a, need) == lib.GEMM_ERR_UNSUPPORTED
+    assert host(a, a, a, a, None, 2, 300, 500, 96, a, need) == lib.GEMM_ERR_UNSUPPORTED
+    assert host(a, a, a, a, None, 2, 300, 500, 64, a, need, cluster=2, cta_group=2) == lib.GEMM_ERR_UNSUPPORTED
     assert host(a, a, a, a, None, 2, 300, 500, 128, a, need, cluster=4, cta_group=2) == lib.GEMM_ERR_UNSUPPORTED
     assert host(a, a, a, a, None, 0, 300, 500, 128, None, 0) == lib.GEMM_OK                     # nothing to do

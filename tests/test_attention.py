@@ -12,31 +12,31 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(b, sq, sk, seed, k_growth=0.0):
+def _inputs(b, sq, sk, seed, k_growth=0.0, d=128):
     from dense_gemm_cluster_gb300 import inputs
-    Q = inputs.bf16_matrix(b * sq, 128, "normal", seed).reshape(b, sq, 128)
-    Kf = inputs.bf16_bits_to_f32(inputs.bf16_matrix(b * sk, 128, "normal", seed + 1)).reshape(b, sk, 128).astype(np.float64)
+    Q = inputs.bf16_matrix(b * sq, d, "normal", seed).reshape(b, sq, d)
+    Kf = inputs.bf16_bits_to_f32(inputs.bf16_matrix(b * sk, d, "normal", seed + 1)).reshape(b, sk, d).astype(np.float64)
     if k_growth:
         # keys grow along the sequence so each key tile raises the row max
         Kf = Kf * (1.0 + k_growth * np.arange(sk)[None, :, None] / sk)
-    K = inputs.f64_to_bf16_bits(Kf).reshape(b, sk, 128)
-    V = inputs.bf16_matrix(b * sk, 128, "normal", seed + 2).reshape(b, sk, 128)
+    K = inputs.f64_to_bf16_bits(Kf).reshape(b, sk, d)
+    V = inputs.bf16_matrix(b * sk, d, "normal", seed + 2).reshape(b, sk, d)
     return Q, K, V
 
 
 def _run(Q, K, V, cluster, out_f32=0, scale=0.0, cta_group=1, causal=False):
     import torch
     from dense_gemm_cluster_gb300 import gemm
-    b, sq, _ = Q.shape
+    b, sq, d = Q.shape
     sk = K.shape[1]
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
-    O = torch.full((b * sq * 128,), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    O = torch.full((b * sq * d,), float("nan"), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
     lse = torch.full((b * sq,), float("nan"), dtype=torch.float32, device="cuda")
-    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, 128, scale, out_f32, cluster, cta_group,
+    s = gemm.attention_forward_run(dev(Q), dev(K), dev(V), O, lse, b, sq, sk, d, scale, out_f32, cluster, cta_group,
                                    causal=causal)
     assert s == gemm.GEMM_OK
     assert gemm.attention_forward_query_status() == gemm.GEMM_OK
-    o = O.float().cpu().numpy().reshape(b, sq, 128).astype(np.float64)
+    o = O.float().cpu().numpy().reshape(b, sq, d).astype(np.float64)
     return o, lse.cpu().numpy().reshape(b, sq).astype(np.float64)
 
 
@@ -85,7 +85,8 @@ def test_attention_argument_errors():
     import torch
     from dense_gemm_cluster_gb300 import gemm
     x = torch.zeros(128 * 128, dtype=torch.int16, device="cuda")
-    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 64) == gemm.GEMM_ERR_UNSUPPORTED
+    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 96) == gemm.GEMM_ERR_UNSUPPORTED
+    assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 64, 0.0, 0, 2, 2) == gemm.GEMM_ERR_UNSUPPORTED
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 3) == gemm.GEMM_ERR_UNSUPPORTED
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 4, 2) == gemm.GEMM_ERR_UNSUPPORTED
     assert gemm.attention_forward_run(x, x, x, x, None, 1, 128, 128, 128, 0.0, 0, 2, 3) == gemm.GEMM_ERR_UNSUPPORTED
@@ -239,3 +240,54 @@ def test_causal_sharing_modes_are_bit_identical():
     for c, g in MODES[1:]:
         o, lse = _run(Q, K, V, c, out_f32=1, cta_group=g, causal=True)
         assert np.array_equal(o, base) and np.array_equal(lse, base_lse), (c, g)
+
+
+MODES_D64 = [(1, 1), (2, 1), (4, 1)]      # the pair MMA needs d = 128
+
+
+@pytest.mark.parametrize("b,sq,sk", [(2, 128, 128), (3, 300, 500), (1, 1000, 130), (1, 77, 1), (2, 1, 300)])
+@pytest.mark.parametrize("cluster,cta_group", MODES_D64)
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_64_matches_oracle(b, sq, sk, cluster, cta_group, causal):
+    # d = 64: one 128-byte swizzle atom per row of Q, K and V; the same kernel otherwise
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    Q, K, V = _inputs(b, sq, sk, 900 + sq, d=64)
+    o, lse = _run(Q, K, V, cluster, out_f32=1, cta_group=cta_group, causal=causal)
+    ref, ref_lse = oracle.attention_forward(Q, K, V, with_lse=True, causal=causal)
+    vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+    assert np.isfinite(o).all()
+    assert np.max(np.abs(o - ref)) <= 1e-2 * vmax
+    assert np.max(np.abs(lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+
+
+def test_head_dim_64_rescales_and_modes_are_bit_identical():
+    import oracle
+    from dense_gemm_cluster_gb300 import inputs
+    Q, K, V = _inputs(2, 512, 1024, 31, k_growth=3.0, d=64)
+    base, base_lse = _run(Q, K, V, 1, out_f32=1, scale=0.2)
+    ref, ref_lse = oracle.attention_forward(Q, K, V, scale=0.2, with_lse=True)
+    vmax = float(np.max(np.abs(inputs.bf16_bits_to_f32(V))))
+    assert np.max(np.abs(base - ref)) <= 1e-2 * vmax
+    assert np.max(np.abs(base_lse - ref_lse) / (1.0 + np.abs(ref_lse))) <= 1e-4
+    for c, g in MODES_D64[1:]:
+        o, lse = _run(Q, K, V, c, out_f32=1, scale=0.2, cta_group=g)
+        assert np.array_equal(o, base) and np.array_equal(lse, base_lse), (c, g)
+
+
+def test_head_dim_64_host_entry_equals_device_entry():
+    import torch
+    from dense_gemm_cluster_gb300 import gemm
+    b, sq, sk = 3, 300, 500
+    Q, K, V = _inputs(b, sq, sk, 41, d=64)
+    ref_o, ref_lse = _run(Q, K, V, 2, out_f32=1, causal=True)
+    host = lambda a: np.ascontiguousarray(a).view(np.int16)
+    O_h = np.full(b * sq * 64, np.nan, dtype=np.float32)
+    lse_h = np.full(b * sq, np.nan, dtype=np.float32)
+    ws_bytes = gemm.attention_forward_host_workspace_bytes(b, sq, sk, 64, 1)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    s = gemm.attention_forward_run_host(host(Q), host(K), host(V), O_h, lse_h, b, sq, sk, 64, ws, ws_bytes, 0.0, 1,
+                                        2, 1, causal=1)
+    assert s == gemm.GEMM_OK
+    assert np.array_equal(O_h.reshape(b, sq, 64).astype(np.float64), ref_o)
+    assert np.array_equal(lse_h.reshape(b, sq).astype(np.float64), ref_lse)
