@@ -57,6 +57,11 @@ WORKLOADS = {
         "gemm4096_bf16_cluster2x2", 4096, 4096, 4096, dist="uniform", layout_a="row", layout_b="col",
         options=dict(mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=2),
         description="GEMM 4096^3 as above with a 2x2 cluster multicasting both A and B"),
+    "gemm4096_bf16_pair2x1": Workload(
+        "gemm4096_bf16_pair2x1", 4096, 4096, 4096, dist="uniform", layout_a="row", layout_b="col",
+        options=dict(cta_group=2, cluster_m=2, cluster_n=1, block_n=256),
+        description="GEMM 4096^3 as above on a 2x1 cluster running the cta_group::2 pair MMA: 256x256 "
+                    "tiles, each CTA loading its 128 rows of A and half of every B tile"),
     "gemm8192_bf16_pair_mcastB4": Workload(
         "gemm8192_bf16_pair_mcastB4", 8192, 8192, 8192, dist="normal", scale=1.0 / math.sqrt(8192),
         out="bf16", beta=0.5,

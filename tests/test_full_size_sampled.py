@@ -30,7 +30,8 @@ def _check_sampled(got_vals, ref_vals, K, out, what):
     assert err <= tolerance(K, out), f"{what}: sampled max|err|/max|ref| = {err:.3e}"
 
 
-@pytest.mark.parametrize("name", ["gemm8192_bf16_pair_mcastB4", "skinny_16384x128x8192", "skinny_128x16384x8192"])
+@pytest.mark.parametrize("name", ["gemm4096_bf16_pair2x1", "gemm8192_bf16_pair_mcastB4", "skinny_16384x128x8192",
+                                  "skinny_128x16384x8192"])
 def test_gemm_workload_full_size_sampled(name):
     import oracle
     from dense_gemm_cluster_gb300 import inputs
