@@ -119,7 +119,21 @@ static gemm_status_t pipe_setup(gemm_handle_t h) {
         e = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_c[i], cudaEventDisableTiming);
     }
-    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "copy pipeline set-up: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) {
+        // release what was created so a later call starts from nothing
+        if (h->pipe_in) cudaStreamDestroy(h->pipe_in);
+        if (h->pipe_out) cudaStreamDestroy(h->pipe_out);
+        for (int i = 0; i < 3; ++i)
+            if (*evs[i]) cudaEventDestroy(*evs[i]);
+        for (int i = 0; i < kHostChunks; ++i) {
+            if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+            if (h->ev_c[i]) cudaEventDestroy(h->ev_c[i]);
+            h->ev_in[i] = h->ev_c[i] = nullptr;
+        }
+        h->pipe_in = h->pipe_out = nullptr;
+        h->ev_start = h->ev_whole = h->ev_out_done = nullptr;
+        return fail(&h->err, GEMM_ERR_CUDA, "copy pipeline set-up: %s", cudaGetErrorString(e));
+    }
     h->pipe_ready = true;
     return GEMM_OK;
 }

@@ -43,7 +43,10 @@
  *     Runs are asynchronous on it unless a call says otherwise.
  *   - Every call returns a gemm_status_t; nothing exits, aborts or throws across
  *     this boundary. On failure, gemm_last_error() holds a one-line reason.
- *   - A handle is used by one host thread at a time.
+ *   - A handle is used by one host thread at a time, and its runs must not
+ *     overlap on the device: launches of one handle share its stream-K
+ *     workspace, tile flags and status word, so runs on different streams need
+ *     an ordering between them (an event, or one handle per stream).
  */
 #ifndef DENSEGEMM_H
 #define DENSEGEMM_H
