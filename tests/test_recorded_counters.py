@@ -48,7 +48,8 @@ def test_multicast_and_pair_cut_measured_l2_to_sm_bytes(records, analytic):
     assert abs(measured / expected - 1.0) < 0.25
 
 
-@pytest.mark.parametrize("name", ["gemm4096_bf16_cluster2x1", "gemm4096_bf16_cluster2x2", "gemm8192_bf16_pair_mcastB4",
+@pytest.mark.parametrize("name", ["gemm4096_bf16_cluster2x1", "gemm4096_bf16_cluster2x2", "gemm4096_bf16_pair2x1",
+                                  "gemm8192_bf16_pair_mcastB4",
                                   "gemm8192_bf16_unicast", "scores_8x16x4096x4096x128", "skinny_16384x128x8192",
                                   "skinny_128x16384x8192"])
 def test_measured_l2_to_sm_bytes_follow_the_analytic_accounting(records, analytic, name):
@@ -73,3 +74,15 @@ def test_dram_traffic_of_bandwidth_sensitive_workloads_stays_near_the_algorithmi
         algorithmic = analytic[name][0].min_hbm_bytes()
     ratio = records[name]["dram_bytes"] / algorithmic
     assert 0.8 <= ratio <= 1.2, f"{name}: DRAM bytes / algorithmic bytes = {ratio:.3f}"
+
+
+def test_pair_and_multicast_share_b_alike_on_4096(records, analytic):
+    # A 2x1 cluster shares B either by multicast (each CTA receives the whole tile) or
+    # through the pair MMA (each CTA loads half); both read B from L2 once per cluster.
+    mc = records["gemm4096_bf16_cluster2x1"]["lts_bytes"]
+    pair = records["gemm4096_bf16_pair2x1"]["lts_bytes"]
+    assert (analytic["gemm4096_bf16_pair2x1"][1].l2_to_sm_operand_bytes ==
+            analytic["gemm4096_bf16_cluster2x1"][1].l2_to_sm_operand_bytes)
+    assert abs(pair / mc - 1.0) < 0.1
+    # the pair also halves what crosses into each SM's shared memory for B
+    assert records["gemm4096_bf16_pair2x1"]["xbar2sm_tma_bytes"] < 0.75 * records["gemm4096_bf16_cluster2x1"]["xbar2sm_tma_bytes"]
