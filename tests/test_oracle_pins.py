@@ -305,6 +305,21 @@ def test_attention_dominant_key_selects_its_value():
         assert np.allclose(O[0, r], val(V[0])[j], rtol=0, atol=1e-30)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_attention_default_scale_is_one_over_sqrt_d(d):
+    # q = e0 and keys 8 e0 and 0: the two scores differ by 8 / sqrt(d) under the default
+    # scale, so with V = (1, 0) the output is the logistic function of that difference
+    # and the log-sum-exp is log(1 + e^(8 / sqrt(d))).
+    Q = np.zeros((1, 1, d)); Q[0, 0, 0] = 1.0
+    K = np.zeros((1, 2, d)); K[0, 0, 0] = 8.0
+    V = np.array([[[1.0], [0.0]]])
+    bits = inputs.f64_to_bf16_bits
+    O, lse = oracle.attention_forward(bits(Q), bits(K), bits(V), with_lse=True)
+    z = 8.0 / math.sqrt(d)
+    assert O[0, 0, 0] == pytest.approx(1.0 / (1.0 + math.exp(-z)), rel=1e-15)
+    assert lse[0, 0] == pytest.approx(math.log1p(math.exp(z)), rel=1e-15)
+
+
 def test_attention_is_invariant_to_key_order_and_keeps_batches_apart():
     Q, K, V = _attn_inputs(2, 6, 23, 16, 12, 530)
     perm = np.random.default_rng(1).permutation(23)
