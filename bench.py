@@ -347,11 +347,12 @@ def bench_ours(args, w: Workload):
         # cluster multicast stays off when several GPUs take part
         opts["mode"] = "unicast"
     g = gemm.Gemm(local, layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out, **opts)
-    s, plan = gemm.gemm_plan(g.options, w.M, w.N, w.K, w.batch, torch.cuda.get_device_properties(device).multi_processor_count)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    s, plan = gemm.gemm_plan(g.options, w.M, w.N, w.K, w.batch, sms)
     g.check(s)
     uni_opts = gemm.make_options(layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out,
                                  block_n=plan.block_n)
-    _, uni_plan = gemm.gemm_plan(uni_opts, w.M, w.N, w.K, w.batch, 148)
+    _, uni_plan = gemm.gemm_plan(uni_opts, w.M, w.N, w.K, w.batch, sms)
 
     p = DeviceProblem(w, device)
     stream = torch.cuda.current_stream(device)

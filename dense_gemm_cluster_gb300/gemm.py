@@ -151,8 +151,8 @@ def gemm_query_status(h, stream=None) -> int:
     return _lib.gemm_query_status(h, _stream(stream))
 
 
-def gemm_plan(opt: gemm_options_t, M, N, K, batch=1, sm_count=148):
-    """Returns (status, gemm_plan_t)."""
+def gemm_plan(opt: gemm_options_t, M, N, K, batch=1, sm_count=152):
+    """Returns (status, gemm_plan_t); sm_count defaults to GB300's 152 SMs."""
     p = gemm_plan_t()
     s = _lib.gemm_plan(ctypes.byref(opt), M, N, K, batch, sm_count, ctypes.byref(p))
     return s, p

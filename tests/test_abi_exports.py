@@ -53,7 +53,7 @@ def test_options_default(lib):
     assert (o.layout_a, o.layout_b, o.layout_c, o.out_type) == (0, 1, 0, 0)
 
 
-def plan(lib, M, N, K, batch=1, sm=148, **kw):
+def plan(lib, M, N, K, batch=1, sm=152, **kw):
     s, p = lib.gemm_plan(lib.make_options(**kw), M, N, K, batch, sm)
     return s, p
 
@@ -64,7 +64,7 @@ def test_plan_4096_cluster2x1(lib):
     assert (p.block_m, p.block_n, p.block_k) == (128, 256, 64)
     assert p.group_a == 1 and p.group_b == 2          # a 2x1 cluster shares only B
     assert p.tiles == (4096 // 256) * (4096 // 256)
-    assert p.clusters == 74
+    assert p.clusters == 76                           # 152 SMs in 2-CTA clusters
     assert p.smem_bytes <= 232448 and p.stages == 4
     from dense_gemm_cluster_gb300 import traffic
     assert p.l2_to_sm_operand_bytes == traffic.l2_to_sm_operand_bytes(4096, 4096, 4096, group_b=2)
