@@ -136,6 +136,7 @@ struct Work {
     int kb0, kb1;
     int kind;
     int contrib_first, contrib_count;   // FINISHER: clusters whose slots hold the rest
+    bool last;                          // the cluster's last work item (no load follows it)
 };
 
 // Cluster launch control ("Clusters, distributed shared memory & cluster launch
@@ -180,6 +181,10 @@ struct WorkIter {
     }
     __device__ long long start_of(long long c) const { return c * base + (c < rem ? c : rem); }
 
+    // The stream-K pieces come first and the whole tiles after them, so a finisher's
+    // wait for its contributors' partials and its fixup overlap the whole tiles'
+    // mainloops instead of ending the kernel. A contributor's piece is always the
+    // first of its range, so every partial is parked at the start.
     __device__ bool next(const KernelParams& p, Work& w) {
         if (clc) {
             long long t = cid;                  // the first tile is this cluster's own
@@ -189,17 +194,19 @@ struct WorkIter {
             w.kb0 = 0;
             w.kb1 = p.num_kb;
             w.kind = WORK_WHOLE;
+            w.last = false;
             return true;
         }
-        if (dp_next < p.dp_tiles) {
+        if (sk_it >= sk_end) {
+            if (dp_next >= p.dp_tiles) return false;
             w.tile = dp_next;
             w.kb0 = 0;
             w.kb1 = p.num_kb;
             w.kind = WORK_WHOLE;
             dp_next += ncl;
+            w.last = dp_next >= p.dp_tiles;
             return true;
         }
-        if (sk_it >= sk_end) return false;
         const long long rel = sk_it / p.num_kb;
         w.tile = p.dp_tiles + rel;
         w.kb0 = (int)(sk_it - rel * p.num_kb);
@@ -218,6 +225,7 @@ struct WorkIter {
             w.kind = WORK_WHOLE;
         }
         sk_it += w.kb1 - w.kb0;
+        w.last = sk_it >= sk_end && dp_next >= p.dp_tiles;
         return true;
     }
 };
@@ -441,8 +449,10 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
 
 // Where a stream-K finisher's epilogue warp stages the partials it adds: its
 // quarter of the operand ring, free once the finisher's last MMA has completed
-// (the finisher is always a cluster's last work item, so no load lands there
-// any more), filled by bulk copies that complete on the warp's own barrier.
+// when the finisher is the cluster's last work item (no load lands there any
+// more), filled by bulk copies that complete on the warp's own barrier. A
+// finisher followed by whole tiles stages nothing (bytes = 0) and adds the
+// partials from global memory while the ring refills.
 struct FixStage {
     uint8_t* ptr;        // generic address of the warp's region
     uint32_t saddr;      // its shared-memory address
@@ -930,13 +940,15 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             const EpiTile et{t_row, n0, m0 + q * 32, row, trow, tc.b, lane, tempty_addr + 8u * acc,
                              w.contrib_first, w.contrib_count, cs, (int)rank};
+            FixStage fsw = fs;
+            if (!w.last) fsw.bytes = 0;                   // loads still land in the ring
             bool stored;
             if (p.out_f32) {
-                if (w.kind == WORK_FINISHER) stored = store_tile<BN, G, true, true>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
-                else                         stored = store_tile<BN, G, true, false>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
+                if (w.kind == WORK_FINISHER) stored = store_tile<BN, G, true, true>(p, &tmC, et, stage_ptr, stage_base, buf, fsw);
+                else                         stored = store_tile<BN, G, true, false>(p, &tmC, et, stage_ptr, stage_base, buf, fsw);
             } else {
-                if (w.kind == WORK_FINISHER) stored = store_tile<BN, G, false, true>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
-                else                         stored = store_tile<BN, G, false, false>(p, &tmC, et, stage_ptr, stage_base, buf, fs);
+                if (w.kind == WORK_FINISHER) stored = store_tile<BN, G, false, true>(p, &tmC, et, stage_ptr, stage_base, buf, fsw);
+                else                         stored = store_tile<BN, G, false, false>(p, &tmC, et, stage_ptr, stage_base, buf, fsw);
             }
             if (!stored) dead = true;
             if (w.kind == WORK_FINISHER) {
