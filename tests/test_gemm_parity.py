@@ -318,3 +318,27 @@ def test_stream_k_finisher_staging_paths(G, K, stages, out):
     b = _run(G, p, 1.0, 0.5, stages=stages)
     assert_close(a, p.reference(1.0, 0.5), K, out, f"finisher staging K={K} stages={stages}")
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("opts", [
+    dict(max_clusters=10),                                                    # single CTAs
+    dict(mode="mcast", mcast_b=1, cluster_m=2, max_clusters=5),               # 2x1 clusters
+    dict(cta_group=2, cluster_m=2, max_clusters=5),                           # pairs
+])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_stream_k_finisher_followed_by_whole_tiles(G, opts, out):
+    # 1024 x 1536 is 48 tiles of 128 x 256 (24 cluster tiles of 256 x 256): on 10 (or 5)
+    # clusters three whole waves run and the last 1.8 waves' tiles are split by k-blocks,
+    # 1.8 tiles' worth per cluster, so ranges start and end inside tiles. Each cluster
+    # runs its split pieces first: a finisher adds its contributors' partials from global
+    # memory while the whole tiles after it stream through the operand ring.
+    p = Problem(1024, 1536, 1000, la="row", lb="col", out=out, beta=0.5, seed=95)
+    a = _run(G, p, 1.0, 0.5, schedule="stream_k", **opts)
+    b = _run(G, p, 1.0, 0.5, schedule="stream_k", **opts)
+    assert_close(a, p.reference(1.0, 0.5), 1000, out, f"stream-K with whole tiles after {opts}")
+    assert np.array_equal(a, b)
+    s, plan = G.gemm_plan(G.make_options(layout_a="row", layout_b="col", out_type=out, schedule="stream_k", **opts),
+                          1024, 1536, 1000, 1, 152)
+    kb = -(-1000 // plan.block_k)
+    assert s == 0 and 0 < plan.stream_k_tiles < plan.tiles
+    assert (plan.stream_k_tiles * kb) % plan.clusters != 0 or (plan.stream_k_tiles * kb // plan.clusters) % kb != 0
