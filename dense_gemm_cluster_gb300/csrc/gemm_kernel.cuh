@@ -558,9 +558,18 @@ __device__ __forceinline__ bool store_tile(const KernelParams& p, const CUtensor
                           ((long long)q * (BN / 4) + (long long)c * (CW / 4)) * 32 + e.lane;
                     stride = 32;
                 }
+                // A partial is read once: let L2 drop it first.
+                uint64_t pol;
+                asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
 #pragma unroll
                 for (int j = 0; j < CW / 4; ++j) {
-                    const float4 a = src[j * stride];
+                    float4 a;
+                    if (per_pass > 0) {
+                        a = src[j * stride];                       // staged: shared memory
+                    } else {
+                        asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                                     : "=f"(a.x), "=f"(a.y), "=f"(a.z), "=f"(a.w) : "l"(src + j * stride), "l"(pol));
+                    }
                     v[4 * j] += a.x;
                     v[4 * j + 1] += a.y;
                     v[4 * j + 2] += a.z;
@@ -909,11 +918,16 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             else        mbar_arrive_local(tempty_addr + 8u * acc);
                         }
                     }
+                    // Kept in L2 at high priority: the finisher reads the partial back
+                    // only after this cluster's whole tiles have streamed their operands.
+                    uint64_t pol;
+                    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        dst[(c * 8 + j) * 32] =
-                            make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;"
+                                     :: "l"(dst + (c * 8 + j) * 32), "f"(__uint_as_float(r[4 * j])),
+                                        "f"(__uint_as_float(r[4 * j + 1])), "f"(__uint_as_float(r[4 * j + 2])),
+                                        "f"(__uint_as_float(r[4 * j + 3])), "l"(pol) : "memory");
                 }
                 __threadfence();
                 epilogue_bar();
