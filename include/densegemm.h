@@ -99,9 +99,10 @@ typedef struct {
     int schedule;       /* 0 = auto, 1 = whole tiles only, 3 = cluster launch control (one
                            cluster per tile; running clusters cancel pending launches and take
                            their tiles, asking for the next tile before computing the current
-                           one), 2 = stream-K tail: the tiles
+                           one), 2 = stream-K: the tiles
                            left after the last full wave (between one and two waves'
-                           worth) are split by k-blocks evenly over all clusters, and the
+                           worth) are split by k-blocks evenly over all clusters, each
+                           cluster runs its split pieces before its whole tiles, and the
                            parts are summed in a fixed order; with fewer tiles than
                            clusters, the k-blocks are spread over more clusters (at least
                            16 k-blocks each). Auto splits the tail when that saves at least
