@@ -203,7 +203,16 @@ def make_options(**kw) -> gemm_options_t:
 
 
 class Gemm:
-    """A handle bound to one device and one set of options."""
+    """A handle bound to one device and one set of options (the fields of gemm_options_t as
+    keywords: mode, mcast_a, mcast_b, cluster_m, cluster_n, cta_group, layout_a/b/c ("row" or
+    "col"), out_type ("bf16" or "f32"), block_n, block_k, stages, max_clusters, group_m,
+    schedule ("auto", "dp", "stream_k", "clc"), wait_timeout_ns, host_parts).
+
+    Buffers are torch tensors or integer addresses (numpy arrays for the host entry points);
+    sizes, leading dimensions and strides are in elements; `stream` is a torch.cuda.Stream, a
+    raw cudaStream_t as an int, or None for the legacy default stream. Every call raises
+    GemmError on a non-OK status. Usable as a context manager (closes the handle).
+    """
 
     def __init__(self, device: int = 0, **options):
         self.options = make_options(**options)
@@ -216,22 +225,29 @@ class Gemm:
             raise GemmError(status, gemm_last_error(self.handle))
 
     def run(self, M, N, K, A, lda, B, ldb, C, ldc, alpha=1.0, beta=0.0, stream=None) -> None:
+        """C <- alpha * A.B + beta * C on device buffers, asynchronously on `stream`."""
         self.check(gemm_run(self.handle, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream))
 
     def run_strided_batched(self, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch, alpha=1.0, beta=0.0,
                             stream=None) -> None:
+        """`batch` GEMMs, operand i at base + i * stride (a stride of 0 shares one operand)."""
         self.check(gemm_run_strided_batched(self.handle, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch,
                                             alpha, beta, stream))
 
     def run_host(self, M, N, K, A, lda, B, ldb, C, ldc, alpha=1.0, beta=0.0, stream=None) -> None:
+        """run() on host buffers (pinned for full speed): the copies in and out are pipelined
+        with the GEMMs, and C holds the result when the call returns."""
         self.check(gemm_run_host(self.handle, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, stream))
 
     def run_strided_batched_host(self, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch, alpha=1.0, beta=0.0,
                                  stream=None) -> None:
+        """run_strided_batched() on host buffers, pipelined over the batch."""
         self.check(gemm_run_strided_batched_host(self.handle, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch,
                                                  alpha, beta, stream))
 
     def query_status(self, stream=None) -> int:
+        """Synchronises `stream` and returns the status of the runs on it (a bounded in-kernel
+        wait that expired reports GEMM_ERR_DEVICE_TIMEOUT)."""
         return gemm_query_status(self.handle, stream)
 
     @property
@@ -242,6 +258,13 @@ class Gemm:
         if self.handle:
             gemm_destroy(self.handle)
             self.handle = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
 
     def __del__(self):
         try:

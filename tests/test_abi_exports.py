@@ -200,3 +200,12 @@ def test_attention_validation_before_launch(lib):
     assert host(a, a, a, a, None, 2, 300, 500, 64, a, need, cluster=2, cta_group=2) == lib.GEMM_ERR_UNSUPPORTED
     assert host(a, a, a, a, None, 2, 300, 500, 128, a, need, cluster=4, cta_group=2) == lib.GEMM_ERR_UNSUPPORTED
     assert host(a, a, a, a, None, 0, 300, 500, 128, None, 0) == lib.GEMM_OK                     # nothing to do
+
+
+def test_gemm_class_rejects_bad_options_before_any_device_call(lib):
+    # resolve() refuses the options before the device is queried, so this needs no GPU
+    with pytest.raises(lib.GemmError) as ei:
+        lib.Gemm(0, cluster_m=16)
+    assert ei.value.status == lib.GEMM_ERR_UNSUPPORTED
+    with pytest.raises(TypeError):
+        lib.Gemm(0, no_such_field=1)
