@@ -209,3 +209,16 @@ def test_gemm_class_rejects_bad_options_before_any_device_call(lib):
     assert ei.value.status == lib.GEMM_ERR_UNSUPPORTED
     with pytest.raises(TypeError):
         lib.Gemm(0, no_such_field=1)
+
+
+def test_gemm_entry_points_refuse_a_null_handle_before_any_cuda_call(lib):
+    a = 1 << 20                                   # fake aligned address, never dereferenced
+    assert lib.gemm_run(None, 8, 8, 8, a, 8, a, 8, a, 8, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_strided_batched(None, 8, 8, 8, a, 8, 64, a, 8, 64, a, 8, 64, 2, 1.0, 0.0) == \
+        lib.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_host(None, 8, 8, 8, a, 8, a, 8, a, 8, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_run_strided_batched_host(None, 8, 8, 8, a, 8, 64, a, 8, 64, a, 8, 64, 2, 1.0, 0.0) == \
+        lib.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_query_status(None) == lib.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_destroy(None) == lib.GEMM_OK
+    assert lib.gemm_launch_count(None) == -1
