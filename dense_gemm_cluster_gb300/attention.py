@@ -67,6 +67,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     args = ap.parse_args(argv)
+    if args.cta_group == 2 and (args.d != 128 or args.cluster not in (None, 2)):
+        ap.error("the pair MMA (--cta-group 2) needs --d 128 and a 2-CTA cluster")
     configs = [(args.cluster, args.cta_group)] if args.cluster else [(1, 1), (2, 1), (4, 1), (2, 2)]
     if args.d != 128:
         configs = [(c, g) for c, g in configs if g == 1]
