@@ -1,6 +1,6 @@
 """Host logic of bench.py without a GPU: the whole-job aggregation over ranks
-(max of elapsed time, sum of work) on a world_size-2 gloo group, and the clock
-sampler's parsing of nvidia-smi CSV."""
+(max of elapsed time, sum of work) on a world_size-2 gloo group, the clock
+sampler's parsing of nvidia-smi CSV, and the reference arm's JSON line."""
 import os
 import socket
 
@@ -53,3 +53,24 @@ def test_clock_sampler_parses_throttle_reasons(tmp_path):
     summ = s.summary()
     assert summ["sm_mhz"] == 1990.0 and summ["sm_max_mhz"] == 2070.0
     assert summ["reasons"] == ["sw_power_cap"] and summ["samples"] == 2
+
+
+def test_reference_arm_prints_one_contract_line_without_a_gpu():
+    # `bench.py --impl reference` times the fp64 oracle on the host cores; it must print one
+    # JSON line with the contract's keys, its own cpu_baseline and a zero-byte e2e.
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "gemm256_f32_mcastB",
+                        "--steps", "2", "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "gemm256_f32_mcastB"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
