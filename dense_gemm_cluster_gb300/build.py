@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libdensegemm.so")
 SOURCES = [os.path.join(CSRC, "gemm_host.cu"), os.path.join(CSRC, "host_io.cu"), os.path.join(CSRC, "tma_bench.cu"), os.path.join(CSRC, "stencil.cu"),
            os.path.join(CSRC, "attention.cu"), os.path.join(CSRC, "attention_host.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "gemm_kernel.cuh"), os.path.join(CSRC, "ptx.cuh"),
-                     os.path.join(CSRC, "gemm_internal.h"),
+                     os.path.join(CSRC, "gemm_internal.h"), os.path.join(CSRC, "host_env.h"),
                      os.path.join(INCLUDE, "densegemm.h"), os.path.join(INCLUDE, "tma_bench.h"),
                      os.path.join(INCLUDE, "stencil.h"), os.path.join(INCLUDE, "attention.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

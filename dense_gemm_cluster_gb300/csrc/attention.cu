@@ -44,6 +44,7 @@
 
 #include "attention.h"
 #include "densegemm.h"
+#include "host_env.h"
 #include "ptx.cuh"
 
 namespace {
@@ -569,6 +570,10 @@ extern "C" gemm_status_t attention_forward_run(const void* Q, const void* K, con
     if (cta_group == 2 && cluster != 2) return afail(GEMM_ERR_UNSUPPORTED, "the pair MMA runs in clusters of 2");
     if (cta_group == 2 && d != 128) return afail(GEMM_ERR_UNSUPPORTED, "the pair MMA needs head dimension 128");
     const bool pair = cta_group == 2;
+    // Clusters of 2 or 4 single-CTA MMAs multicast every K/V tile: single-GPU only.
+    if (cluster > 1 && !pair && dgc_host::world_is_multi_gpu())
+        return afail(GEMM_ERR_UNSUPPORTED,
+                     "K/V cluster multicast is single-GPU only; WORLD_SIZE > 1 requires cluster 1 or the pair MMA");
     if (!Q || !K || !V || !O) return afail(GEMM_ERR_INVALID_ARG, "null pointer");
     if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
          reinterpret_cast<uintptr_t>(O) | reinterpret_cast<uintptr_t>(lse)) & 15u)

@@ -12,6 +12,7 @@
 #include <cstdint>
 
 #include "attention.h"
+#include "host_env.h"
 
 namespace {
 
@@ -85,6 +86,7 @@ extern "C" gemm_status_t attention_forward_run_host(const void* Q, const void* K
     if ((d != 64 && d != 128) || (cluster != 1 && cluster != 2 && cluster != 4) || (cta_group != 1 && cta_group != 2) ||
         (cta_group == 2 && (cluster != 2 || d != 128)))
         return GEMM_ERR_UNSUPPORTED;
+    if (cluster > 1 && cta_group == 1 && dgc_host::world_is_multi_gpu()) return GEMM_ERR_UNSUPPORTED;   // multicast
     if (!Q || !K || !V || !O || !workspace) return GEMM_ERR_INVALID_ARG;
     const Layout l = layout_for(batch, sq, sk, d, out_f32);
     if (workspace_bytes < l.total) return GEMM_ERR_INVALID_ARG;

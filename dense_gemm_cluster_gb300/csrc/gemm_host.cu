@@ -17,6 +17,7 @@
 
 #include "densegemm.h"
 #include "gemm_internal.h"
+#include "host_env.h"
 #include "gemm_kernel.cuh"
 
 namespace dgc_host {
@@ -282,11 +283,6 @@ extern "C" gemm_status_t gemm_plan(const gemm_options_t* opt, int64_t M, int64_t
                                                              r.pub.cluster_m * r.pub.cluster_n);
     }
     return s;
-}
-
-static bool world_is_multi_gpu() {
-    const char* w = getenv("WORLD_SIZE");
-    return w && atoi(w) > 1;
 }
 
 extern "C" gemm_status_t gemm_create(gemm_handle_t* out, const gemm_options_t* opt, int device) {
@@ -641,6 +637,13 @@ gemm_status_t dgc_host::run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t 
         kp.flags = h->flags;
     }
     cfg.numAttrs = o.schedule == 3 ? 1 : 2;
+    if (h->no_alloc) {
+        // The shared static record must start at zero; cleared only now, when every
+        // check has passed and a launch follows, so a refused call writes nothing.
+        cudaError_t e = cudaMemsetAsync(h->d_status, 0, 16, stream);
+        if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "clearing the status record: %s", cudaGetErrorString(e));
+        h->status_cleared = true;
+    }
     void* args[] = {&tmA, &tmB, &tmC, &kp};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "cudaLaunchKernelEx: %s", cudaGetErrorString(e));
@@ -703,8 +706,8 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[256];
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = sizeof(g_noalloc_scratch);
 constexpr size_t kStatusRecordBytes = 16;
+static_assert(kStatusRecordBytes <= sizeof(g_noalloc_scratch), "the static array must hold one status record");
 constexpr int kMaxDevices = 64;
 
 struct NoAllocDevice {
@@ -758,9 +761,14 @@ extern "C" gemm_status_t gemm_run_noalloc(const gemm_options_t* opt, int device,
                                           uint32_t* status_out) {
     if (!opt) return fail(nullptr, GEMM_ERR_INVALID_ARG, "gemm_run_noalloc needs options");
     if (device < 0 || device >= kMaxDevices) return fail(nullptr, GEMM_ERR_INVALID_ARG, "bad device %d", device);
-    if (kStatusRecordBytes > kNoAllocScratchBytes)
-        return fail(nullptr, GEMM_ERR_UNSUPPORTED, "a launch needs %zu bytes of static scratch; the array holds %zu",
-                    kStatusRecordBytes, kNoAllocScratchBytes);
+    // Options and sizes first: an impossible request is refused before the device is touched.
+    {
+        Resolved r;
+        gemm_status_t s = resolve(*opt, M, N, K, 1, 1, r, nullptr);
+        if (s != GEMM_OK) return s;
+    }
+    if (opt->schedule == 2)
+        return fail(nullptr, GEMM_ERR_UNSUPPORTED, "the stream-K tail needs a workspace; gemm_run_noalloc runs whole tiles");
     if (opt->mode == GEMM_MODE_MCAST && (opt->mcast_a || opt->mcast_b) && world_is_multi_gpu())
         return fail(nullptr, GEMM_ERR_UNSUPPORTED,
                     "cluster multicast is single-GPU only; WORLD_SIZE > 1 requires unicast or the pair MMA");
@@ -781,14 +789,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const gemm_options_t* opt, int device,
         memcpy(local.smem_set, d.smem_set, sizeof local.smem_set);
         memcpy(local.occ_key, d.occ, sizeof local.occ_key);
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int prev = 0;
-    cudaGetDevice(&prev);
-    if (prev != device) cudaSetDevice(device);
-    // The record must start at zero: earlier calls leave their contents behind.
-    cudaError_t e = cudaMemsetAsync(local.d_status, 0, kStatusRecordBytes, st);
-    if (prev != device) cudaSetDevice(prev);
-    if (e != cudaSuccess) return fail(nullptr, GEMM_ERR_CUDA, "clearing the status record: %s", cudaGetErrorString(e));
+    // run_impl clears the record on `stream` right before the GEMM kernel's launch
+    // (and only then: an empty problem or K = 0 launches no GEMM and writes no record).
     gemm_status_t s = run_impl(&local, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, alpha, beta, stream);
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mutex);
@@ -801,8 +803,16 @@ extern "C" gemm_status_t gemm_run_noalloc(const gemm_options_t* opt, int device,
         return s;
     }
     if (status_out) {
+        if (!local.status_cleared) {
+            // No GEMM kernel ran, so no wait could expire; the record was not touched.
+            memset(status_out, 0, kStatusRecordBytes);
+            return GEMM_OK;
+        }
+        int prev = 0;
+        cudaGetDevice(&prev);
         if (prev != device) cudaSetDevice(device);
-        e = cudaMemcpyAsync(status_out, local.d_status, kStatusRecordBytes, cudaMemcpyDeviceToHost, st);
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaMemcpyAsync(status_out, local.d_status, kStatusRecordBytes, cudaMemcpyDeviceToHost, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         if (prev != device) cudaSetDevice(prev);
         if (e != cudaSuccess) return fail(nullptr, GEMM_ERR_CUDA, "reading the status record: %s", cudaGetErrorString(e));

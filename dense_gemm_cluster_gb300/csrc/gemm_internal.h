@@ -42,6 +42,7 @@ struct gemm_handle_s {
     cudaEvent_t ev_in[dgc_host::kHostChunks] = {}, ev_c[dgc_host::kHostChunks] = {};
     int64_t launches = 0;
     bool no_alloc = false;      // set on the stack handle of gemm_run_noalloc: never allocate
+    bool status_cleared = false;// gemm_run_noalloc: the launch path cleared the static record (a GEMM kernel followed)
     float* workspace = nullptr; // stream-K partial slots
     unsigned int* flags = nullptr;
     size_t workspace_bytes = 0;

@@ -15,6 +15,7 @@
 #include <cstring>
 
 #include "densegemm.h"
+#include "host_env.h"
 #include "ptx.cuh"
 #include "tma_bench.h"
 
@@ -231,6 +232,8 @@ extern "C" gemm_status_t tma_bench_run(const tma_bench_options_t* opt, const voi
     if (c != 1 && c != 2 && c != 4 && c != 8) return bench_fail(GEMM_ERR_UNSUPPORTED, "cluster must be 1, 2, 4 or 8");
     if (c == 1) mode = TMA_BENCH_UNICAST;
     if (mode < 0 || mode > 2) return bench_fail(GEMM_ERR_INVALID_ARG, "bad mode");
+    if (mode != TMA_BENCH_UNICAST && dgc_host::world_is_multi_gpu())
+        return bench_fail(GEMM_ERR_UNSUPPORTED, "cluster multicast is single-GPU only; WORLD_SIZE > 1 requires unicast");
     if (o.box_rows < 8 || o.box_rows > 256 || o.box_rows % 8) return bench_fail(GEMM_ERR_UNSUPPORTED, "box_rows 8..256, multiple of 8");
     if (mode == TMA_BENCH_MULTICAST_SLICED && (o.box_rows % (8 * c)))
         return bench_fail(GEMM_ERR_UNSUPPORTED, "sliced multicast needs box_rows a multiple of 8*cluster");

@@ -149,7 +149,11 @@ void gemm_options_default(gemm_options_t *opt);
  * multicast slice under 8 rows) and for any multicast mode when the environment
  * variable WORLD_SIZE is above 1 (multi-GPU jobs run without cluster multicast).
  * The handle owns a 16-byte device status word and, once needed, the stream-K
- * workspace and the gemm_run_host staging buffers; gemm_destroy frees them. */
+ * workspace and the gemm_run_host staging buffers; gemm_destroy frees them.
+ * Defined by: the launch set-up of "Clusters, distributed shared memory &
+ * cluster launch control", section "Thread-block clusters" (cluster shape as a
+ * launch attribute) and the tensor-map descriptors of "Hopper TMA Multicast
+ * 深度解析与实测", section 实测 Microbenchmark 源码实现; the mode is fixed here. */
 gemm_status_t gemm_create(gemm_handle_t *out, const gemm_options_t *opt, int device);
 
 /* C <- alpha * op(A) * op(B) + beta * C on `stream`, asynchronously.
@@ -158,7 +162,11 @@ gemm_status_t gemm_create(gemm_handle_t *out, const gemm_options_t *opt, int dev
  * propagate). M, N or K == 0 is valid: K == 0 gives C <- beta * C.
  * Requirements, checked before any launch: A, B, C 16-byte aligned; lda*2,
  * ldb*2 and ldc*sizeof(C element) multiples of 16 bytes (GEMM_ERR_ALIGNMENT);
- * ld at least the contiguous extent; every dimension below 2^31. */
+ * ld at least the contiguous extent; every dimension below 2^31.
+ * Defined by: the contraction itself ("Clusters, distributed shared memory &
+ * cluster launch control", section "Where these plug into the GEMM": the tiled
+ * GEMM whose CTAs share operand tiles); the operand sharing it runs with is the
+ * handle's mode ("Hopper TMA Multicast 深度解析与实测", section 核心架构认知). */
 gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                        const void *A, int64_t lda, const void *B, int64_t ldb,
                        void *C, int64_t ldc, float alpha, float beta, void *stream);
@@ -169,7 +177,9 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * that strideA or strideB may be 0: one matrix serves every product. Overlapping
  * strides return GEMM_ERR_INVALID_ARG. The attention-score form is
  * A = Q (row-major, sq x d), B = K^T (K given row-major sk x d is B column-major
- * with ldb = d), C = S (fp32, sq x sk). */
+ * with ldb = d), C = S (fp32, sq x sk).
+ * Defined by: "Hopper TMA Multicast 深度解析与实测", section 经典应用场景 (S_i =
+ * Q_i K^T for the query tiles of one head, every CTA reading the same K tile). */
 gemm_status_t gemm_run_strided_batched(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                                        const void *A, int64_t lda, int64_t strideA,
                                        const void *B, int64_t ldb, int64_t strideB,
@@ -207,7 +217,10 @@ gemm_status_t gemm_run_strided_batched_host(gemm_handle_t h, int64_t M, int64_t 
 
 /* Synchronizes `stream`, then reads and clears the device status word.
  * GEMM_ERR_DEVICE_TIMEOUT if a bounded wait expired in any run since the last
- * query (gemm_last_error() then names the role, stage and CTA). */
+ * query (gemm_last_error() then names the role, stage and CTA).
+ * Defined by: "Hopper TMA Multicast 深度解析与实测", section 深度机制剖析 (a
+ * receiver's mbarrier waits for bytes another CTA announced; here every such
+ * wait is bounded and its expiry is reported instead of hanging). */
 gemm_status_t gemm_query_status(gemm_handle_t h, void *stream);
 
 /* Host-only planning: validates `opt` and the problem as gemm_run would and
@@ -215,7 +228,7 @@ gemm_status_t gemm_query_status(gemm_handle_t h, void *stream);
 gemm_status_t gemm_plan(const gemm_options_t *opt, int64_t M, int64_t N, int64_t K,
                         int64_t batch, int sm_count, gemm_plan_t *plan);
 
-/* Static string for a status code. */
+/* Static string for a status code. (Library plumbing; no page passage.) */
 const char *gemm_status_string(gemm_status_t s);
 
 /* The last failure reason recorded on this handle (or by gemm_create / gemm_plan
@@ -234,16 +247,20 @@ int64_t gemm_launch_count(gemm_handle_t h);
  * no handle and allocates nothing (no cudaMalloc, cudaFree or allocating library
  * routine). Its status record lives in a 256-byte static device array that the
  * library holds on every GPU that loads it until the process exits; a launch
- * uses 16 bytes of it, and a launch needing more than the array holds is
- * rejected with GEMM_ERR_UNSUPPORTED.
+ * uses 16 bytes of it (a size fixed when the library is compiled, and checked
+ * against the array's size at compile time). Whole tiles only: the stream-K
+ * schedule (schedule 2), which needs a workspace, returns GEMM_ERR_UNSUPPORTED.
  *   - Same arguments and semantics as gemm_create + gemm_run, with the options
  *     and the device given directly; the caller passes A, B and C (device memory).
  *   - The first call on each device does a one-time set-up with that device
  *     current (it looks up the array's device address and the driver's
  *     tensor-map encoder); make that first call before any stream capture.
+ *   - Options and sizes are checked before the device is touched; every
+ *     argument error returns before anything is enqueued.
  *   - Every call shares the one array and clears the status record on `stream`
- *     before its launch. Calls whose kernels overlap on the GPU race on it, so
- *     a timeout seen by one may be reported to another.
+ *     right before its GEMM kernel's launch (a call that launches no GEMM kernel,
+ *     such as K = 0 or an empty C, leaves it alone). Calls whose kernels overlap
+ *     on the GPU race on it, so a timeout seen by one may be reported to another.
  *   - status_out: NULL for a fully asynchronous call; otherwise a host array of
  *     4 uint32 that receives the status record after the call synchronizes
  *     `stream` (GEMM_ERR_DEVICE_TIMEOUT if a bounded wait expired). */
@@ -252,7 +269,9 @@ gemm_status_t gemm_run_noalloc(const gemm_options_t *opt, int device, int64_t M,
                                void *C, int64_t ldc, float alpha, float beta, void *stream,
                                uint32_t *status_out);
 
-/* Frees the handle and everything it owns. Safe on NULL. */
+/* Frees the handle and everything it owns. Safe on NULL. (Library plumbing; the
+ * kernel-side teardown it pairs with follows "集群编程", section 同步: no CTA
+ * leaves while a peer may still address its shared memory.) */
 gemm_status_t gemm_destroy(gemm_handle_t h);
 
 #ifdef __cplusplus

@@ -58,7 +58,9 @@ typedef struct {
  * grid size actually used is returned in *ctas_used). Also reports the bytes
  * that land in shared memory (delivered) and that the TMA units fetch (issued):
  * with multicast, issued = delivered / cluster. A bounded wait that expires is
- * reported by tma_bench_query_status. */
+ * reported by tma_bench_query_status. The multicast modes are single-GPU only:
+ * with the WORLD_SIZE environment variable above 1 they return
+ * GEMM_ERR_UNSUPPORTED before any CUDA call. */
 gemm_status_t tma_bench_run(const tma_bench_options_t *opt, const void *src, int64_t rows, int64_t cols,
                             int64_t ld, uint64_t *cycles, uint64_t *ns, uint32_t *verify,
                             int *ctas_used, double *delivered_bytes, double *issued_bytes,

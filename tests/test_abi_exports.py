@@ -222,3 +222,43 @@ def test_gemm_entry_points_refuse_a_null_handle_before_any_cuda_call(lib):
     assert lib.gemm_query_status(None) == lib.GEMM_ERR_INVALID_ARG
     assert lib.gemm_destroy(None) == lib.GEMM_OK
     assert lib.gemm_launch_count(None) == -1
+
+
+def test_multicast_refused_in_a_multi_gpu_job_before_any_cuda_call(lib, monkeypatch):
+    # Cluster-multicast TMA loads are single-GPU only. With WORLD_SIZE > 1 every entry
+    # point that would issue them refuses before touching the device (no GPU here; the
+    # fake addresses are never dereferenced).
+    a = 1 << 20
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert lib.attention_forward_run(a, a, a, a, None, 1, 256, 256, 128, 0.0, 0, 2, 1) == lib.GEMM_ERR_UNSUPPORTED
+    assert lib.attention_forward_run(a, a, a, a, None, 1, 256, 256, 64, 0.0, 0, 4, 1) == lib.GEMM_ERR_UNSUPPORTED
+    need = lib.attention_forward_host_workspace_bytes(2, 300, 500, 128, 0)
+    assert lib.attention_forward_run_host(a, a, a, a, None, 2, 300, 500, 128, a, need, cluster=2) == \
+        lib.GEMM_ERR_UNSUPPORTED
+    for mode in (1, 2):
+        o = lib.tma_bench_options_t(mode=mode, cluster=2, ctas=0, box_rows=128, stages=4, iters=8, warmup=0,
+                                    streaming_stride=0, wait_timeout_ns=0)
+        s, *_ = lib.tma_bench_run(o, a, 4096, 4096, 4096, a, a, a)
+        assert s == lib.GEMM_ERR_UNSUPPORTED and "single-GPU" in lib.tma_bench_last_error()
+    mc = lib.make_options(mode="mcast", mcast_b=1, cluster_m=2)
+    assert lib.gemm_run_noalloc(mc, 0, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == lib.GEMM_ERR_UNSUPPORTED
+    assert "WORLD_SIZE" in lib.gemm_last_error(None)
+    with pytest.raises(lib.GemmError) as ei:
+        lib.Gemm(0, mode="mcast", mcast_b=1, cluster_m=2)
+    assert ei.value.status == lib.GEMM_ERR_UNSUPPORTED
+
+
+def test_noalloc_checks_options_before_the_device(lib):
+    # Impossible options and sizes come back as such (not as a CUDA error) without a GPU:
+    # gemm_run_noalloc validates before its one-time device set-up.
+    a = 1 << 20
+    run = lib.gemm_run_noalloc
+    assert run(lib.make_options(cluster_m=16), 0, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == \
+        lib.GEMM_ERR_UNSUPPORTED
+    assert run(lib.make_options(cta_group=2, cluster_m=1), 0, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == \
+        lib.GEMM_ERR_UNSUPPORTED
+    assert run(lib.make_options(schedule="stream_k"), 0, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == \
+        lib.GEMM_ERR_UNSUPPORTED
+    assert "workspace" in lib.gemm_last_error(None)
+    assert run(lib.make_options(), 0, -1, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
+    assert run(lib.make_options(), 99, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
