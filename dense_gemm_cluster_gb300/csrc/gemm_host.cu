@@ -358,6 +358,38 @@ extern "C" gemm_status_t gemm_destroy(gemm_handle_t h) {
 
 extern "C" int64_t gemm_launch_count(gemm_handle_t h) { return h ? h->launches : -1; }
 
+extern "C" int64_t gemm_schedule_work(int64_t tiles, int64_t dp_tiles, int num_kb, int64_t clusters,
+                                      int64_t cluster, gemm_work_item_t* items, int64_t capacity) {
+    if (tiles < 0 || dp_tiles < 0 || dp_tiles > tiles || num_kb < 1 || clusters < 1 || cluster < 0 ||
+        cluster >= clusters || capacity < 0 || (capacity > 0 && !items))
+        return -1;
+    // The same iterator the kernel's roles walk, replayed on the host.
+    dgc::KernelParams kp;
+    memset(&kp, 0, sizeof kp);
+    kp.num_kb = num_kb;
+    kp.total_tiles = tiles;
+    kp.dp_tiles = dp_tiles;
+    kp.sk_iters = (tiles - dp_tiles) * (int64_t)num_kb;
+    dgc::WorkIter wi;
+    wi.init(kp, cluster, clusters, nullptr);
+    dgc::Work w;
+    int64_t n = 0;
+    while (wi.next(kp, w)) {
+        if (n < capacity) {
+            gemm_work_item_t& it = items[n];
+            it.tile = w.tile;
+            it.kb0 = w.kb0;
+            it.kb1 = w.kb1;
+            it.kind = w.kind;
+            it.contrib_first = w.kind == dgc::WORK_FINISHER ? w.contrib_first : -1;
+            it.contrib_count = w.kind == dgc::WORK_FINISHER ? w.contrib_count : 0;
+            it.last = w.last ? 1 : 0;
+        }
+        ++n;
+    }
+    return n;
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Encodes a 3-D tiled map (inner, outer, batch) with the 128-byte swizzle.

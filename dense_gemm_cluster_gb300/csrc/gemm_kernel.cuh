@@ -90,8 +90,9 @@ struct KernelParams {
     long long ldc, stride_c; // elements
     unsigned int* status;    // 4 words: code, detail, block, tile
     unsigned long long timeout_ns;
-    // Stream-K tail: tiles [0, dp_tiles) go whole to clusters by a static stride;
-    // the sk_iters k-blocks of the remaining tiles are split evenly over the clusters.
+    // Stream-K split: tiles [0, dp_tiles) go whole to clusters by a static stride;
+    // the sk_iters k-blocks of the remaining tiles are split evenly over the clusters
+    // (each cluster runs its split pieces before its whole tiles).
     long long dp_tiles;
     long long sk_iters;
     float* workspace;        // one BLOCK_M x BN fp32 partial slot per CTA of the grid
@@ -104,7 +105,7 @@ struct TileCoord {
     int b, ctm, ctn;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const KernelParams& p, long long t) {
+__host__ __device__ __forceinline__ TileCoord tile_coord(const KernelParams& p, long long t) {
     const long long per_batch = (long long)p.tiles_m * p.tiles_n;
     TileCoord c;
     c.b = (int)(t / per_batch);
@@ -112,7 +113,7 @@ __device__ __forceinline__ TileCoord tile_coord(const KernelParams& p, long long
     const long long in_group = (long long)p.group_m * p.tiles_n;
     const int group = (int)(r / in_group);
     const int first_m = group * p.group_m;
-    const int gsz = min(p.group_m, p.tiles_m - first_m);
+    const int gsz = p.group_m < p.tiles_m - first_m ? p.group_m : p.tiles_m - first_m;
     const int local = (int)(r - (long long)group * in_group);
     c.ctm = first_m + local % gsz;
     c.ctn = local / gsz;
@@ -158,17 +159,20 @@ struct ClcCtx {
 
 __device__ bool clc_next(const KernelParams& p, ClcCtx& c, long long& tile);
 
-// Static persistent schedule with a stream-K tail ("Clusters, distributed
+// Static persistent schedule with a stream-K split ("Clusters, distributed
 // shared memory & cluster launch control", section "The second wall": a fixed
 // stride leaves SMs idle in the last wave when tiles do not divide evenly;
-// splitting the last tiles' k-blocks evenly removes that tail). Every role of
-// every CTA of a cluster walks the same sequence.
+// splitting the last waves' k-blocks evenly over all clusters removes that
+// idle time). Every role of every CTA of a cluster walks the same sequence.
+// Compiled for the host too, where gemm_schedule_work replays it so that the
+// partition can be checked without a GPU.
 struct WorkIter {
     long long dp_next, sk_it, sk_end, cid, ncl, base, rem;
     ClcCtx* clc = nullptr;   // set: tiles come from cluster launch control
     bool first_done = false;
 
-    __device__ void init(const KernelParams& p, long long cluster, long long clusters, ClcCtx* ctx = nullptr) {
+    __host__ __device__ void init(const KernelParams& p, long long cluster, long long clusters,
+                                  ClcCtx* ctx = nullptr) {
         clc = p.clc ? ctx : nullptr;
         first_done = false;
         cid = cluster;
@@ -179,16 +183,20 @@ struct WorkIter {
         sk_it = start_of(cluster);
         sk_end = start_of(cluster + 1);
     }
-    __device__ long long start_of(long long c) const { return c * base + (c < rem ? c : rem); }
+    __host__ __device__ long long start_of(long long c) const { return c * base + (c < rem ? c : rem); }
 
     // The stream-K pieces come first and the whole tiles after them, so a finisher's
     // wait for its contributors' partials and its fixup overlap the whole tiles'
     // mainloops instead of ending the kernel. A contributor's piece is always the
     // first of its range, so every partial is parked at the start.
-    __device__ bool next(const KernelParams& p, Work& w) {
+    __host__ __device__ bool next(const KernelParams& p, Work& w) {
         if (clc) {
             long long t = cid;                  // the first tile is this cluster's own
+#ifdef __CUDA_ARCH__
             if (first_done && !clc_next(p, *clc, t)) return false;
+#else
+            if (first_done) return false;       // cluster launch control has no host form
+#endif
             first_done = true;
             w.tile = t;
             w.kb0 = 0;

@@ -88,6 +88,29 @@ _lib.gemm_run_noalloc.argtypes = [_OPT_P, _i32, _i64, _i64, _i64, _vp, _i64, _vp
 _lib.gemm_run_noalloc.restype = _i32
 
 
+class gemm_work_item_t(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int64), ("kb0", ctypes.c_int32), ("kb1", ctypes.c_int32),
+                ("kind", ctypes.c_int32), ("contrib_first", ctypes.c_int32), ("contrib_count", ctypes.c_int32),
+                ("last", ctypes.c_int32)]
+
+
+_lib.gemm_schedule_work.argtypes = [_i64, _i64, _i32, _i64, _i64, ctypes.POINTER(gemm_work_item_t), _i64]
+_lib.gemm_schedule_work.restype = _i64
+
+WORK_WHOLE, WORK_PARTIAL, WORK_FINISHER = 0, 1, 2
+
+
+def gemm_schedule_work(tiles, dp_tiles, num_kb, clusters, cluster):
+    """The work units one cluster of a persistent launch walks (host-only), as a list of
+    (tile, kb0, kb1, kind, contrib_first, contrib_count, last) tuples."""
+    n = _lib.gemm_schedule_work(tiles, dp_tiles, num_kb, clusters, cluster, None, 0)
+    if n < 0:
+        raise ValueError("gemm_schedule_work: invalid arguments")
+    buf = (gemm_work_item_t * max(1, n))()
+    _lib.gemm_schedule_work(tiles, dp_tiles, num_kb, clusters, cluster, buf, n)
+    return [(it.tile, it.kb0, it.kb1, it.kind, it.contrib_first, it.contrib_count, it.last) for it in buf[:n]]
+
+
 def library_path() -> str:
     return _LIB_PATH
 

@@ -269,6 +269,27 @@ gemm_status_t gemm_run_noalloc(const gemm_options_t *opt, int device, int64_t M,
                                void *C, int64_t ldc, float alpha, float beta, void *stream,
                                uint32_t *status_out);
 
+/* One unit of a persistent cluster's work (host-only schedule diagnostic). */
+typedef struct {
+    int64_t tile;          /* cluster tile id (before the raster's mapping to block rows/columns) */
+    int32_t kb0, kb1;      /* k-blocks [kb0, kb1) of the tile */
+    int32_t kind;          /* 0 whole tile, 1 partial (parks an fp32 partial), 2 finisher */
+    int32_t contrib_first; /* finisher: first cluster whose partial it adds (else -1) */
+    int32_t contrib_count; /* finisher: number of such clusters, consecutive (else 0) */
+    int32_t last;          /* 1 on the cluster's last unit */
+} gemm_work_item_t;
+
+/* Host-only: the units cluster `cluster` of a persistent launch walks, in order,
+ * for `tiles` cluster tiles of `num_kb` k-blocks on `clusters` clusters, the first
+ * `dp_tiles` (a multiple of `clusters` as the planner chooses it) handed out whole
+ * by a static stride and the k-blocks of the rest split evenly over all clusters
+ * (stream-K, "Clusters, distributed shared memory & cluster launch control",
+ * section "The second wall"). The same iterator the kernel runs, compiled for the
+ * host. Writes at most `capacity` items and returns how many there are, or -1 for
+ * invalid arguments. Needs no GPU. */
+int64_t gemm_schedule_work(int64_t tiles, int64_t dp_tiles, int num_kb, int64_t clusters, int64_t cluster,
+                           gemm_work_item_t *items, int64_t capacity);
+
 /* Frees the handle and everything it owns. Safe on NULL. (Library plumbing; the
  * kernel-side teardown it pairs with follows "集群编程", section 同步: no CTA
  * leaves while a peer may still address its shared memory.) */
