@@ -187,6 +187,98 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
 
 
+class NvmlClocks:
+    """SM clock, power and clock-event reasons of this process's GPU, polled every
+    `period_s` on a background thread through NVML's read-only queries (ctypes on
+    libnvidia-ml; nothing is set). Samples carry a wall-clock time, so a summary can
+    be taken over any window (the timed steps, the sustained region)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device, period_s: float = 0.001):
+        import ctypes
+        import threading
+        self.period_s = period_s
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            self.ok = self._find_handle(device)
+            self._u = ctypes.c_uint()
+            self._ull = ctypes.c_ulonglong()
+            self._reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1,
+                                                                                 ctypes.byref(mx)) == 0 else None
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _find_handle(self, device) -> bool:
+        import ctypes
+        import torch
+        props = torch.cuda.get_device_properties(device)
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            u = str(uuid)
+            for cand in (u, "GPU-" + u):
+                if self.lib.nvmlDeviceGetHandleByUUID(cand.encode(), ctypes.byref(self.handle)) == 0:
+                    return True
+        if hasattr(props, "pci_bus_id"):
+            bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle)) == 0:
+                return True
+        return False
+
+    def _poll(self):
+        import ctypes
+        lib, h, u, ull = self.lib, self.handle, self._u, self._ull
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            mhz = float(u.value) if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(u)) == 0 else None
+            mw = float(u.value) if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(u)) == 0 else None
+            rs = int(ull.value) if self._reasons_fn(h, ctypes.byref(ull)) == 0 else 0
+            if mhz is not None:
+                self.samples.append((t, mhz, None if mw is None else mw / 1e3, rs))
+            self._stop.wait(self.period_s)
+
+    def __enter__(self):
+        import threading
+        if self.ok:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            time.sleep(0.01)
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if self.ok:
+            self.lib.nvmlShutdown()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [r for r in self.samples if t0 <= r[0] <= t1]
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        sm = [r[1] for r in rows]
+        pw = [r[2] for r in rows if r[2] is not None]
+        bits = 0
+        for r in rows:
+            bits |= r[3]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_mhz_min": min(sm) if sm else None,
+                "sm_mhz_max_seen": max(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(pw) if pw else None, "power_w_median": statistics.median(pw) if pw else None,
+                "samples": len(sm), "period_ms": self.period_s * 1e3, "window_s": t1 - t0,
+                "reasons": sorted(n for b, n in self.REASONS.items() if bits & b), "source": "nvml, in process"}
+
+
 # ---------------------------------------------------------------- inputs on the device
 class DeviceProblem:
     """The workload's operands, generated on the host from the seed and copied to HBM once."""
@@ -287,6 +379,36 @@ def oracle_rate(w: Workload, budget_s: float, seed: int = 0):
     return rows * per_row_flops / t / 1e12, t, rows, oracle.num_threads()
 
 
+def single_core_oracle(name: str) -> dict:
+    """The oracle on one host core over a whole small workload (the 256^3 GEMM is quoted as
+    "CPU oracle in seconds"): a child process with OMP_NUM_THREADS=1, best of 3 runs."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-core", name], env=env,
+                             capture_output=True, text=True, timeout=300, check=True).stdout
+        return json.loads(out.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, OSError, ValueError, IndexError) as e:
+        return {"workload": name, "error": str(e)[:200]}
+
+
+def oracle_one_core_main(name: str) -> int:
+    import oracle
+    oracle.build()
+    w = WORKLOADS[name]
+    assert w.batch == 1 and w.beta == 0.0
+    A, lda = inputs.store(inputs.bf16_matrix(w.M, w.K, w.dist, inputs.STREAM_A, w.scale), w.layout_a)
+    B, ldb = inputs.store(inputs.bf16_matrix(w.K, w.N, w.dist, inputs.STREAM_B, w.scale), w.layout_b)
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        oracle.gemm(w.M, w.N, w.K, A, lda, w.layout_a, B, ldb, w.layout_b)
+        times.append(time.perf_counter() - t0)
+    t = min(times)
+    print(json.dumps({"workload": name, "seconds": t, "gflops": w.flops / t / 1e9, "threads": oracle.num_threads(),
+                      "runs": 3, "what": "whole product, fp64 oracle, best of 3"}))
+    return 0
+
+
 # ---------------------------------------------------------------- arms
 def bench_reference(args, w: Workload):
     world, rank, _ = dist_env()
@@ -332,6 +454,50 @@ def bench_reference(args, w: Workload):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def l2_to_sm_report(w: Workload, plan, uni_plan, traffic_rec) -> dict:
+    """The multicast evidence: L2 -> SM operand bytes of this launch against the same output
+    computed with unicast tiles, analytic (the planner's accounting) and measured (ncu
+    lts__t_sectors_srcunit_tex_op_read of both launches, each record taken on the current
+    kernel sources; null when either record is missing or stale)."""
+    from dense_gemm_cluster_gb300.workloads import UNICAST_TWIN
+    twin = UNICAST_TWIN.get(w.name)
+    twin_rec = recorded_traffic(twin) if twin else None
+    mine = traffic_rec.get("lts_bytes") if traffic_rec else None
+    theirs = twin_rec.get("lts_bytes") if twin_rec else None
+    return {"analytic": plan.l2_to_sm_operand_bytes,
+            "analytic_unicast": uni_plan.l2_to_sm_operand_bytes,
+            "reduction_vs_unicast": uni_plan.l2_to_sm_operand_bytes / max(1, plan.l2_to_sm_operand_bytes),
+            "measured": mine, "unicast_workload": twin, "measured_unicast": theirs,
+            "reduction_measured": (theirs / mine) if (mine and theirs) else None,
+            "counter": "ncu lts__t_sectors_srcunit_tex_op_read.sum x 32 B, one launch each (profiles/ncu_traffic.json)"}
+
+
+def sustained_region(g, copies, stream, steps, region_s, seconds, device, flops_per_step):
+    """Repeats the K-step region back to back for about `seconds`, each region between
+    its own pair of events on the launching stream. Returns (wall start, wall end,
+    summary of the per-region rates)."""
+    import math
+    import torch
+    n = max(2, min(20000, math.ceil(seconds / max(region_s, 1e-6))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    launches0 = g.launches
+    t0 = time.perf_counter()
+    for r in range(n):
+        evs[r][0].record(stream)
+        for i in range(steps):
+            run_once(g, copies[i % len(copies)], stream)
+        evs[r][1].record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.perf_counter()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    tf = sorted(flops_per_step * steps / (m / 1e3) / 1e12 for m in ms)
+    q = lambda f: tf[min(len(tf) - 1, int(f * len(tf)))]
+    return t0, t1, {"regions": n, "steps_per_region": steps, "launches": g.launches - launches0,
+                    "seconds_gpu": sum(ms) / 1e3, "tflops_median": statistics.median(tf), "tflops_min": tf[0],
+                    "tflops_p10": q(0.1), "tflops_p90": q(0.9), "tflops_max": tf[-1],
+                    "note": "after the reported steps, not part of value"}
 
 
 def bench_ours(args, w: Workload):
@@ -387,7 +553,9 @@ def bench_ours(args, w: Workload):
     launches0 = g.launches
     barrier(dist)
     torch.cuda.synchronize(device)
-    with ClockSampler(local) as clk:
+    nv = NvmlClocks(device)
+    sustained = None
+    with (nv if nv.ok else ClockSampler(local)) as clk:
         wall0 = time.perf_counter()
         if not needs_flush:
             starts[0].record(stream)
@@ -402,12 +570,18 @@ def bench_ours(args, w: Workload):
         if not needs_flush:
             ends[0].record(stream)
         torch.cuda.synchronize(device)
-        wall = time.perf_counter() - wall0
-    barrier(dist)
-    launches = g.launches - launches0
+        wall1 = time.perf_counter()
+        wall = wall1 - wall0
+        barrier(dist)
+        launches = g.launches - launches0
+        step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+        local_s = sum(step_ms) / 1e3
+        if args.sustain_s > 0 and not needs_flush:
+            # After the reported steps: the same K-step region repeated back to back for
+            # about sustain_s, each region between its own events, to see the rate and the
+            # clocks under sustained load (power cap) beside the reported burst.
+            sustained = sustained_region(g, copies, stream, args.steps, local_s, args.sustain_s, device, w.flops)
     g.check(g.query_status(stream))
-    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
-    local_s = sum(step_ms) / 1e3
     elapsed, units = aggregate(dist, local_s, float(w.flops) * args.steps, device)
     value = units / elapsed / 1e12
     ms_per_step = 1e3 * elapsed / args.steps
@@ -429,7 +603,23 @@ def bench_ours(args, w: Workload):
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "peak_source": f"hbm_gbs (copy) of {peaks_kind}",
                     "algorithmic_bytes_per_launch": w.min_hbm_bytes()}
-    clocks = clk.summary()
+    clocks = clk.summary(wall0, wall1) if nv.ok else clk.summary()
+    if sustained is not None:
+        t0, t1, sus = sustained
+        sus["clocks"] = nv.summary(t0, t1) if nv.ok else None
+        if roofline["bound"] == "tensor":
+            sus_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+            sus.update({"frac_of_sustained_peak": sus["tflops_median"] / sus_peak, "sustained_peak": sus_peak,
+                        "frac_of_burst_peak": sus["tflops_median"] / tensor_peak,
+                        "peak_source": f"bf16_tflops_sustained and bf16_tflops of {peaks_kind}"})
+        else:
+            gbs = sus["tflops_median"] * 1e12 / w.flops * w.min_hbm_bytes() / 1e9
+            sus.update({"hbm_gbs_median": gbs, "frac_of_hbm_peak": gbs / hbm_peak,
+                        "peak_source": f"hbm_gbs of {peaks_kind}"})
+        roofline["sustained"] = sus
+    if roofline["bound"] == "tensor":
+        sus_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        roofline.update({"sustained_peak": sus_peak, "frac_of_sustained_peak": achieved / sus_peak})
     if roofline["bound"] == "tensor":
         rated = rated_tensor_peak(device, clocks)
         roofline.update({"rated_peak": rated["tflops"], "frac_of_rated": achieved / rated["tflops"],
@@ -459,11 +649,7 @@ def bench_ours(args, w: Workload):
                            f"back to back between one pair of events")),
                    "description": w.description},
         "roofline": roofline,
-        "l2_to_sm_operand_bytes": {"analytic": plan.l2_to_sm_operand_bytes,
-                                   "analytic_unicast": uni_plan.l2_to_sm_operand_bytes,
-                                   "reduction_vs_unicast": uni_plan.l2_to_sm_operand_bytes /
-                                   max(1, plan.l2_to_sm_operand_bytes),
-                                   "measured": traffic_rec.get("lts_bytes") if traffic_rec else None},
+        "l2_to_sm_operand_bytes": l2_to_sm_report(w, plan, uni_plan, traffic_rec),
         "gpu_launches": launches,
         "wall_s_timed_region": wall,
         "clocks": clocks,
@@ -475,7 +661,8 @@ def bench_ours(args, w: Workload):
         rate, secs, rows, threads = oracle_rate(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": f"rows 0..{rows - 1} of C ({rows}x{w.N}x{w.K}"
-                                          f"{', first batch' if w.batch > 1 else ''}) in {secs:.1f} s"}
+                                          f"{', first batch' if w.batch > 1 else ''}) in {secs:.1f} s",
+                                "single_core_256": single_core_oracle("gemm256_f32_mcastB")}
     g.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -738,9 +925,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back repeats of the timed region after it (rate and clocks under "
+                         "sustained load; 0 = none)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch count of a batched workload (smaller profiling captures)")
+    ap.add_argument("--oracle-one-core", metavar="WORKLOAD", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.oracle_one_core:
+        return oracle_one_core_main(args.oracle_one_core)
     if args.warmup < 3:
         args.warmup = 3
     if args.workload in ATTENTION_WORKLOADS:

@@ -62,6 +62,11 @@ WORKLOADS = {
         options=dict(cta_group=2, cluster_m=2, cluster_n=1, block_n=256),
         description="GEMM 4096^3 as above on a 2x1 cluster running the cta_group::2 pair MMA: 256x256 "
                     "tiles, each CTA loading its 128 rows of A and half of every B tile"),
+    "gemm4096_bf16_unicast": Workload(
+        "gemm4096_bf16_unicast", 4096, 4096, 4096, dist="uniform", layout_a="row", layout_b="col",
+        options=dict(mode="unicast", cluster_m=1, cluster_n=1, cta_group=1, block_n=256),
+        description="GEMM 4096^3 as above with unicast loads and single-CTA 128x256 tiles (the baseline for "
+                    "the 4096^3 sharing modes' L2->SM operand-byte comparison)"),
     "gemm8192_bf16_pair_mcastB4": Workload(
         "gemm8192_bf16_pair_mcastB4", 8192, 8192, 8192, dist="normal", scale=1.0 / math.sqrt(8192),
         out="bf16", beta=0.5,
@@ -91,7 +96,17 @@ WORKLOADS = {
         description="skinny GEMM M=128, N=16384, K=8192, U(-1,1), bf16 out, small A multicast along N"),
 }
 
-DEFAULT = "gemm4096_bf16_cluster2x1"
+# The bench's default: the largest single-GPU GEMM, on the pair MMA with 4-CTA B multicast.
+DEFAULT = "gemm8192_bf16_pair_mcastB4"
+
+# The unicast workload that computes the same output with every CTA fetching its own
+# tiles: the measured L2->SM operand bytes of a sharing mode are compared with it.
+UNICAST_TWIN = {
+    "gemm4096_bf16_cluster2x1": "gemm4096_bf16_unicast",
+    "gemm4096_bf16_cluster2x2": "gemm4096_bf16_unicast",
+    "gemm4096_bf16_pair2x1": "gemm4096_bf16_unicast",
+    "gemm8192_bf16_pair_mcastB4": "gemm8192_bf16_unicast",
+}
 
 
 @dataclass(frozen=True)

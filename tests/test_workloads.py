@@ -20,7 +20,6 @@ def test_gemm_4096_uniform_a_row_b_col_bf16_on_a_2x1_cluster():
     assert w.dist == "uniform" and (w.layout_a, w.layout_b) == ("row", "col") and w.out == "bf16"
     assert (w.alpha, w.beta) == (1.0, 0.0)
     assert w.options == dict(mode="mcast", mcast_a=1, mcast_b=1, cluster_m=2, cluster_n=1)
-    assert DEFAULT == w.name                       # the bench's default workload
     pair = WORKLOADS["gemm4096_bf16_pair2x1"]      # the same problem on a pair
     assert (pair.M, pair.N, pair.K, pair.dist, pair.layout_a, pair.layout_b, pair.out) == \
         (w.M, w.N, w.K, w.dist, w.layout_a, w.layout_b, w.out)
@@ -37,6 +36,18 @@ def test_gemm_8192_scaled_normal_pair_tiles_b_multicast_beta_half():
     uni = WORKLOADS["gemm8192_bf16_unicast"]       # the comparison: same problem, unicast tiles
     assert (uni.M, uni.N, uni.K, uni.dist, uni.scale, uni.beta) == (w.M, w.N, w.K, w.dist, w.scale, w.beta)
     assert uni.options["mode"] == "unicast" and uni.options.get("cta_group", 1) == 1
+    assert DEFAULT == w.name                       # the bench's default: the largest single-GPU GEMM
+
+
+def test_unicast_twins_compute_the_same_output():
+    from dense_gemm_cluster_gb300.workloads import UNICAST_TWIN
+    for name, twin in UNICAST_TWIN.items():
+        w, u = WORKLOADS[name], WORKLOADS[twin]
+        same = lambda x: (x.M, x.N, x.K, x.batch, x.dist, x.scale, x.layout_a, x.layout_b, x.layout_c, x.out,
+                          x.alpha, x.beta)
+        assert same(w) == same(u)
+        assert u.options["mode"] == "unicast" and u.options.get("cta_group", 1) == 1
+        assert u.options.get("cluster_m", 1) == 1 and u.options.get("cluster_n", 1) == 1
 
 
 def test_attention_scores_8x16_heads_4096_by_4096_by_128_fp32():
