@@ -38,6 +38,12 @@
 // wall"), rastered in bands of group_m cluster-rows so that co-running
 // clusters share A and B tiles in L2.
 //
+// L2 traffic: when the tile grid is one tile wide, the operand that each tile
+// reads alone is loaded with an evict-first policy and the one every tile reads
+// with evict-last (K-major streamed rows also start at a tile-dependent k-block);
+// each producer prefetches its first stages into L2 before waiting for the
+// previous grid in the stream (programmatic dependent launch).
+//
 // Every wait is bounded by wait_timeout_ns of %globaltimer; on expiry the
 // thread records a status word in global memory, raises a CTA-wide abort flag
 // and its role stops, so the kernel always returns.
@@ -99,7 +105,12 @@ struct KernelParams {
     unsigned int* flags;     // per slot: 1 while the slot holds a partial not yet summed, else 0
     int clc;                 // 1: one cluster per tile; running clusters take pending ones' tiles
     int a_shared, b_shared;  // 1: one matrix serves every product of the batch (stride 0)
+    int a_l2, b_l2;          // L2 eviction priority of the operand's loads: 0 none, 1 evict first, 2 evict last
+    int k_rotate;            // 1: whole tiles start their k walk at a tile-dependent k-block
+    int prefetch;            // 1: prefetch the first stages into L2 before waiting for the previous grid
 };
+
+enum : int { L2_HINT_NONE = 0, L2_HINT_EVICT_FIRST = 1, L2_HINT_EVICT_LAST = 2 };
 
 struct TileCoord {
     int b, ctm, ctn;
@@ -309,6 +320,16 @@ __device__ __forceinline__ uint32_t col_mask(int rx, int ry, int cx) {
     return m;
 }
 
+// Whole tiles may start their k walk at a tile-dependent k-block (wrapping around),
+// so that concurrent tiles do not all ask L2 for the same k-block of the operand they
+// share. Returns the offset for work `w` (0: in order).
+__device__ __forceinline__ int k_rotation(const KernelParams& p, const Work& w) {
+    const int nkb = w.kb1 - w.kb0;
+    if (!p.k_rotate || w.kind != WORK_WHOLE || nkb < 2) return 0;
+    const long long t = w.tile;
+    return (int)(((t * (long long)nkb) / (p.total_tiles > 0 ? p.total_tiles : 1) + t) % nkb);
+}
+
 // One operand's producer loop (run by one thread). Per k-block (BK wide): wait
 // until the stage is released by every CTA this thread writes into, arm each
 // receiver's full barrier with the bytes of this thread's slice (through mapa
@@ -335,7 +356,27 @@ struct OperandPlan {
 
 template <int G, int BK>
 __device__ __forceinline__ void tma_issue(const OperandPlan& op, bool mcast, uint32_t dst, uint32_t bar, int x, int y,
-                                          int z, int w, bool four_d) {
+                                          int z, int w, bool four_d, bool hint, uint64_t pol) {
+    if (hint) {
+        if (four_d) {
+            if (G == 1) {
+                if (mcast) tma_load_4d_mcast_hint(dst, op.tmap, bar, x, y, z, w, (uint16_t)op.mask, pol);
+                else       tma_load_4d_hint(dst, op.tmap, bar, x, y, z, w, pol);
+            } else {
+                if (mcast) tma_load_4d_pair_mcast_hint(dst, op.tmap, bar, x, y, z, w, (uint16_t)op.mask, pol);
+                else       tma_load_4d_pair_hint(dst, op.tmap, bar, x, y, z, w, pol);
+            }
+        } else {
+            if (G == 1) {
+                if (mcast) tma_load_3d_mcast_hint(dst, op.tmap, bar, x, y, z, (uint16_t)op.mask, pol);
+                else       tma_load_3d_hint(dst, op.tmap, bar, x, y, z, pol);
+            } else {
+                if (mcast) tma_load_3d_pair_mcast_hint(dst, op.tmap, bar, x, y, z, (uint16_t)op.mask, pol);
+                else       tma_load_3d_pair_hint(dst, op.tmap, bar, x, y, z, pol);
+            }
+        }
+        return;
+    }
     if (four_d) {
         if (G == 1) {
             if (mcast) tma_load_4d_mcast(dst, op.tmap, bar, x, y, z, w, (uint16_t)op.mask);
@@ -351,6 +392,68 @@ __device__ __forceinline__ void tma_issue(const OperandPlan& op, bool mcast, uin
         } else {
             if (mcast) tma_load_3d_pair_mcast(dst, op.tmap, bar, x, y, z, (uint16_t)op.mask);
             else       tma_load_3d_pair(dst, op.tmap, bar, x, y, z);
+        }
+    }
+}
+
+// This issuer's part of a stage's tile (see the layouts above).
+struct SliceGeom {
+    int atom0, r0, k_rows;
+    uint32_t slice_off;      // byte offset of the part within the tile
+};
+
+template <int BK>
+__device__ __forceinline__ SliceGeom slice_geom(const OperandPlan& op) {
+    constexpr int NAT = BK / ATOM_K;
+    SliceGeom g{0, 0, BK, 0u};
+    if (op.mn_major) {
+        g.k_rows = BK / op.parts;
+        g.slice_off = (uint32_t)(op.slice * g.k_rows * 128);
+    } else if (op.kmap4) {
+        if (op.parts <= NAT) {
+            g.atom0 = op.slice * (NAT / op.parts);
+        } else {
+            const int rparts = op.parts / NAT;
+            g.atom0 = op.slice / rparts;
+            g.r0 = (op.slice % rparts) * (op.rows / rparts);
+        }
+        g.slice_off = (uint32_t)(g.atom0 * op.rows * 128 + g.r0 * 128);
+    } else {
+        g.r0 = op.slice * (op.rows / op.parts);
+        g.slice_off = (uint32_t)(g.r0 * 128);
+    }
+    return g;
+}
+
+// Prefetches into L2 this issuer's part of the first stages of its cluster's first
+// work item: the same boxes produce() will load, so a launch that follows another in
+// the stream overlaps its first DRAM reads with the previous grid's last tiles. A
+// prefetch returns no data to the SM, so it may run before griddepcontrol.wait.
+template <int G, int BK>
+__device__ __forceinline__ void prefetch_first_stages(const KernelParams& p, const OperandPlan& op, bool is_a, int cx,
+                                                      int cy, int rx, int ry, int BNv, int BN_CTAv, long long cluster,
+                                                      long long clusters, int S) {
+    constexpr int NAT = BK / ATOM_K;
+    WorkIter wi;
+    wi.init(p, cluster, clusters, nullptr);
+    Work w;
+    if (!wi.next(p, w)) return;
+    const SliceGeom sg = slice_geom<BK>(op);
+    const TileCoord tc = tile_coord(p, w.tile);
+    const int zb = op.shared ? 0 : tc.b;
+    const int mn0 = is_a ? (tc.ctm * cx + rx) * BLOCK_M
+                         : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
+    const int nkb = w.kb1 - w.kb0;
+    const int rot = k_rotation(p, w);
+    for (int i = 0; i < S && i < nkb; ++i) {
+        const int kb = w.kb0 + (i + rot < nkb ? i + rot : i + rot - nkb);
+        if (op.mn_major) {
+            const int y = kb * BK + op.slice * sg.k_rows;
+            for (int box = 0; box < op.rows / 64; ++box) tma_prefetch_3d(op.tmap, mn0 + box * 64, y, zb);
+        } else if (op.kmap4) {
+            tma_prefetch_4d(op.tmap, 0, mn0 + sg.r0, kb * NAT + sg.atom0, zb);
+        } else {
+            tma_prefetch_3d(op.tmap, kb * BK, mn0 + sg.r0, zb);
         }
     }
 }
@@ -372,26 +475,13 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     const uint32_t slice_bytes = op.tile_bytes / (uint32_t)op.parts;
     const uint32_t tma_bar0 = (G == 2) ? mapa(full0, leader) : full0;
     const bool mcast = op.parts > 1;
-    // This issuer's part of the tile.
-    int atom0 = 0, r0 = 0, k_rows = BK;
-    uint32_t slice_off;
-    if (op.mn_major) {
-        k_rows = BK / op.parts;
-        slice_off = (uint32_t)(op.slice * k_rows * 128);
-    } else if (op.kmap4) {
-        if (op.parts <= NAT) {
-            atom0 = op.slice * (NAT / op.parts);
-        } else {
-            const int rparts = op.parts / NAT;
-            atom0 = op.slice / rparts;
-            r0 = (op.slice % rparts) * (op.rows / rparts);
-        }
-        slice_off = (uint32_t)(atom0 * op.rows * 128 + r0 * 128);
-    } else {
-        r0 = op.slice * (op.rows / op.parts);
-        slice_off = (uint32_t)(r0 * 128);
-    }
+    const SliceGeom sg = slice_geom<BK>(op);
     bool extra_tx = is_a && (p.debug_flags & 1) != 0;
+    // L2 eviction priority of this operand's loads (chosen by the planner).
+    const int l2 = is_a ? p.a_l2 : p.b_l2;
+    const bool hint = l2 != L2_HINT_NONE;
+    const uint64_t pol = l2 == L2_HINT_EVICT_FIRST ? l2_policy_evict_first()
+                       : l2 == L2_HINT_EVICT_LAST  ? l2_policy_evict_last() : 0ull;
     int stage = 0;
     uint32_t phase = 0;
     WorkIter wi;
@@ -417,7 +507,10 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
         const int zb = op.shared ? 0 : tc.b;           // batch coordinate of this operand
         const int mn0 = is_a ? (tc.ctm * cx + rx) * BLOCK_M
                              : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        const int nkb = w.kb1 - w.kb0;
+        const int rot = k_rotation(p, w);
+        for (int i = 0; i < nkb; ++i) {
+            const int kb = w.kb0 + (i + rot < nkb ? i + rot : i + rot - nkb);
             if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, p, abort_flag, ERR_WAIT_EMPTY, (uint32_t)stage, t))
                 return false;
 #pragma unroll
@@ -431,16 +524,16 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
                 extra_tx = false;
             }
             const uint32_t bar = tma_bar0 + 8u * stage;
-            const uint32_t dst = op.tile0 + stage * op.tile_bytes + slice_off;
+            const uint32_t dst = op.tile0 + stage * op.tile_bytes + sg.slice_off;
             if (op.mn_major) {
-                const int y = kb * BK + op.slice * k_rows;
+                const int y = kb * BK + op.slice * sg.k_rows;
                 for (int box = 0; box < op.rows / 64; ++box)
                     tma_issue<G, BK>(op, mcast, dst + (uint32_t)(box * BK * 128), bar, mn0 + box * 64, y, zb, 0,
-                                     false);
+                                     false, hint, pol);
             } else if (op.kmap4) {
-                tma_issue<G, BK>(op, mcast, dst, bar, 0, mn0 + r0, kb * NAT + atom0, zb, true);
+                tma_issue<G, BK>(op, mcast, dst, bar, 0, mn0 + sg.r0, kb * NAT + sg.atom0, zb, true, hint, pol);
             } else {
-                tma_issue<G, BK>(op, mcast, dst, bar, kb * BK, mn0 + r0, zb, 0, false);
+                tma_issue<G, BK>(op, mcast, dst, bar, kb * BK, mn0 + sg.r0, zb, 0, false, hint, pol);
             }
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -753,11 +846,19 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // and touch no global memory (operands, C, workspace, flags, status) before the
     // previous grid has completed and its writes are visible. Both are no-ops for a
     // launch without the attribute.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
     const long long cluster = cluster_id_x();
     const long long clusters = num_clusters_x();
+    // The producers' operand plans (A: warp 0, B: warp 6).
+    OperandPlan op;
+    if (warp == 0) op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, p.a_kmap4, idxA, gA, maskA,
+                                    p.a_shared};
+    else           op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB,
+                                    p.b_shared};
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p.prefetch && (warp == 0 || warp == 6) && lane == 0)
+        prefetch_first_stages<G, BK>(p, op, warp == 0, cx, cy, rx, ry, BN, BN_CTA, cluster, clusters, S);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     ClcCtx clc_ctx;
     clc_ctx.resp0 = ring_resp0;
     clc_ctx.full0 = smem_u32(&ring_full[0]);
@@ -771,16 +872,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // ------------------------------------------------------------ producers (A: warp 0, B: warp 6)
         if (lane == 0) {
             const bool is_a = warp == 0;
-            OperandPlan op;
-            if (is_a) {
-                prefetch_tmap(&tmA);
-                op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, p.a_kmap4, idxA, gA, maskA,
-                                 p.a_shared};
-            } else {
-                prefetch_tmap(&tmB);
-                op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB,
-                                 p.b_shared};
-            }
+            prefetch_tmap(is_a ? static_cast<const void*>(&tmA) : static_cast<const void*>(&tmB));
             produce<G, BK>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
                        BN, BN_CTA, abort_flag, cluster, clusters, S, &clc_ctx, smem_u32(&ring_empty[0]));
         }
@@ -827,7 +919,7 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                           ERR_WAIT_TMEM_EMPTY, acc, t)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {     // stages arrive in the producers' k order
                     if (!wait_bounded(smem_u32(&full_bar[stage]), phase, p, abort_flag,
                                       ERR_WAIT_FULL, (uint32_t)stage, t)) { ok = false; break; }
                     tc_fence_after();

@@ -229,6 +229,88 @@ __device__ __forceinline__ void tma_load_4d_pair_mcast(uint32_t dst, const void*
         " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
         :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask) : "memory");
 }
+// The same loads with an L2 eviction-priority policy (from createpolicy) attached.
+#define DGC_TMA_HINT ".L2::cache_hint"
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes" DGC_TMA_HINT
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_mcast_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                       int32_t x, int32_t y, int32_t z, uint16_t mask, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        DGC_TMA_HINT " [%0], [%1, {%3, %4, %5}], [%2], %6, %7;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                      int32_t x, int32_t y, int32_t z, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes" DGC_TMA_HINT
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_mcast_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                            int32_t x, int32_t y, int32_t z, uint16_t mask,
+                                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster" DGC_TMA_HINT " [%0], [%1, {%3, %4, %5}], [%2], %6, %7;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z, int32_t w, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes" DGC_TMA_HINT
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_mcast_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                       int32_t x, int32_t y, int32_t z, int32_t w, uint16_t mask,
+                                                       uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        DGC_TMA_HINT " [%0], [%1, {%3, %4, %5, %6}], [%2], %7, %8;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                      int32_t x, int32_t y, int32_t z, int32_t w, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes" DGC_TMA_HINT
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair_mcast_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                            int32_t x, int32_t y, int32_t z, int32_t w, uint16_t mask,
+                                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster" DGC_TMA_HINT " [%0], [%1, {%3, %4, %5, %6}], [%2], %7, %8;"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask), "l"(pol) : "memory");
+}
+// L2 eviction-priority policies covering every access they are attached to.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// Bring a tile of global memory into L2 without delivering it anywhere (a hint:
+// it returns no data, so it may run before a previous grid's writes are visible).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 :: "l"(tmap), "r"(x), "r"(y), "r"(z) : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 :: "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
 // 3-D tiled store from this CTA's shared memory (clipped at the tensor bounds).
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
                                              int32_t x, int32_t y, int32_t z) {

@@ -92,8 +92,9 @@ WORKLOADS = {
                     "multicast along M across the two pairs of a 4-CTA cluster"),
     "skinny_128x16384x8192": Workload(
         "skinny_128x16384x8192", 128, 16384, 8192, dist="uniform",
-        options=dict(mode="mcast", mcast_a=1, cluster_m=1, cluster_n=4, block_n=128),
-        description="skinny GEMM M=128, N=16384, K=8192, U(-1,1), bf16 out, small A multicast along N"),
+        options=dict(mode="mcast", mcast_a=1, cluster_m=1, cluster_n=2, block_n=128),
+        description="skinny GEMM M=128, N=16384, K=8192, U(-1,1), bf16 out, small A multicast along N across "
+                    "the 2 CTAs of a cluster"),
 }
 
 # The bench's default: the largest single-GPU GEMM, on the pair MMA with 4-CTA B multicast.

@@ -137,6 +137,11 @@ typedef struct {
     int64_t clusters;   /* persistent grid size in clusters (before the occupancy cap) */
     int64_t l2_to_sm_operand_bytes; /* analytic TMA operand fetches for the launch */
     int64_t stream_k_tiles;   /* tiles split by k-blocks (0: whole tiles only) */
+    int l2_hint_a, l2_hint_b; /* L2 eviction priority of A's / B's loads (the operands as launched,
+                                 after the column-major-C transpose): 0 none, 1 evict first (each
+                                 tile of it is read by one cluster tile only), 2 evict last (read
+                                 by every cluster tile) */
+    int k_rotate;             /* 1: whole tiles start their k walk at a tile-dependent k-block */
 } gemm_plan_t;
 
 /* Default options: unicast, 1x1 cluster, cta_group 1, A row-major, B column-major,

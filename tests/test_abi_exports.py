@@ -262,3 +262,29 @@ def test_noalloc_checks_options_before_the_device(lib):
     assert "workspace" in lib.gemm_last_error(None)
     assert run(lib.make_options(), 0, -1, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
     assert run(lib.make_options(), 99, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
+
+
+def test_plan_l2_hints_and_k_rotation(lib):
+    # One tile along N: A streams once (evict first), B is read by every tile (evict last),
+    # and K-major A rows start at tile-dependent k-blocks.
+    s, p = plan(lib, 16384, 128, 8192, layout_a="row", layout_b="row", cta_group=2, cluster_m=4, block_n=128,
+                mode="mcast", mcast_b=1)
+    assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (1, 2, 1)
+    # One tile along M: the mirror; a row-major (MN-major) B is walked in lockstep.
+    s, p = plan(lib, 128, 16384, 8192, layout_a="row", layout_b="row", block_n=128)
+    assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (2, 1, 0)
+    s, p = plan(lib, 128, 16384, 8192, layout_a="row", layout_b="col", block_n=128)
+    assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (2, 1, 0)
+    s, p = plan(lib, 16384, 128, 8192, layout_a="col", layout_b="row", block_n=128)
+    assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (1, 2, 0)     # MN-major A: in order
+    # Column-major C runs C^T = B^T A^T: the launched operands swap roles.
+    s, p = plan(lib, 16384, 128, 8192, layout_a="row", layout_b="row", layout_c="col", block_n=128)
+    assert s == 0 and p.transposed == 1 and (p.l2_hint_a, p.l2_hint_b) == (2, 1)
+    # Tiles along both dimensions, or a batch: no hints, no rotation.
+    for args, kw in [((8192, 8192, 8192), dict(cta_group=2, cluster_m=4, mode="mcast", mcast_b=1)),
+                     ((4096, 4096, 4096), dict(cluster_m=2, mode="mcast", mcast_b=1)),
+                     ((128, 128, 8192), dict())]:
+        s, p = plan(lib, *args, **kw)
+        assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (0, 0, 0), args
+    s, p = plan(lib, 4096, 4096, 128, batch=128, layout_b="col", cluster_m=4, mode="mcast", mcast_b=1)
+    assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (0, 0, 0)

@@ -5,7 +5,7 @@ cta_group 1 here (unicast and cluster multicast); the pair MMA has its own file.
 import numpy as np
 import pytest
 
-from gpu_cases import Problem, assert_close, decode, options_for, sample_positions
+from gpu_cases import Problem, assert_close, decode, options_for
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +80,22 @@ def test_cluster_modes_match_oracle_and_unicast_bitwise(G, cm, cn, ma, mb, bn):
     assert_close(got, p.reference(), 448, "bf16", f"cluster {cm}x{cn} mcast A{ma} B{mb}")
     # multicast moves the same operand bytes: the product is bit-identical
     assert np.array_equal(got, uni)
+
+
+@pytest.mark.parametrize("opts", [dict(block_n=128),
+                                  dict(cta_group=2, cluster_m=4, mode="mcast", mcast_b=1, block_n=128),
+                                  dict(block_n=128, schedule="stream_k", max_clusters=6)])
+def test_rotated_k_walk_with_l2_hints_matches_oracle(G, opts):
+    # One tile along N: the planner streams A with an evict-first policy, keeps the B that
+    # every tile reads with evict-last, and starts each whole tile's k walk at its own
+    # k-block, wrapping around. K = 1000 leaves a partial last k-block, which the rotated
+    # walk must still load exactly once; the stream-K case mixes split pieces (in order)
+    # with rotated whole tiles.
+    p = Problem(1536, 100, 1000, la="row", lb="row", out="f32", seed=97)
+    s, plan = G.gemm_plan(G.make_options(**options_for(p, **opts)), p.M, p.N, p.K, 1, 152)
+    assert s == 0 and (plan.k_rotate, plan.l2_hint_a, plan.l2_hint_b) == (1, 1, 2)
+    got = _run(G, p, **opts)
+    assert_close(got, p.reference(), p.K, "f32", f"rotated k walk {opts}")
 
 
 @pytest.mark.parametrize("lb", ["row", "col"])

@@ -1,7 +1,7 @@
 """The persistent kernel's work partition, replayed on the host (no GPU).
 
 ``gemm_schedule_work`` runs the kernel's own work iterator compiled for the host.
-Over thousands of (tiles, whole tiles, k-blocks, clusters) shapes these tests
+Over hundreds of (tiles, whole tiles, k-blocks, clusters) shapes these tests
 check what the stream-K finisher waits rely on ("Clusters, distributed shared
 memory & cluster launch control", section "The second wall": the k-blocks of
 the last waves are split evenly over every cluster):
