@@ -49,7 +49,7 @@ def test_multicast_and_pair_cut_measured_l2_to_sm_bytes(records, analytic):
 
 
 @pytest.mark.parametrize("name", ["gemm4096_bf16_cluster2x1", "gemm4096_bf16_cluster2x2", "gemm4096_bf16_pair2x1",
-                                  "gemm8192_bf16_pair_mcastB4",
+                                  "gemm4096_bf16_unicast", "gemm8192_bf16_pair_mcastB4",
                                   "gemm8192_bf16_unicast", "scores_8x16x4096x4096x128", "skinny_16384x128x8192",
                                   "skinny_128x16384x8192"])
 def test_measured_l2_to_sm_bytes_follow_the_analytic_accounting(records, analytic, name):
@@ -102,3 +102,29 @@ def test_l2_resident_gemm_reads_its_inputs_once_plus_the_stream_k_partials(recor
     assert 0.8 * w.min_hbm_bytes() <= got <= 1.05 * (w.min_hbm_bytes() + 2 * partials), (
         f"{name}: {got / 1e6:.1f} MB of DRAM traffic against {w.min_hbm_bytes() / 1e6:.1f} MB of inputs and "
         f"output and {partials / 1e6:.1f} MB of partial slots")
+
+
+def test_every_workload_has_a_record_taken_on_the_current_kernel_sources(records):
+    # bench.py reports `traffic` and the measured L2 -> SM reduction only from records whose
+    # source hash matches the kernels being built; every workload must have one.
+    import bench
+    from dense_gemm_cluster_gb300.workloads import ATTENTION_WORKLOADS, WORKLOADS
+    gemm_sha = bench.kernel_source_hash()
+    attn_sha = bench.kernel_source_hash(bench.ATTN_KERNEL_SOURCES)
+    for name in WORKLOADS:
+        assert records[name]["kernel_sha"] == gemm_sha, f"{name}: counters taken on other kernel sources"
+        assert bench.recorded_traffic(name) is not None
+    name = "attention_fwd_8x16x4096x4096x128"
+    assert name in ATTENTION_WORKLOADS and records[name]["kernel_sha"] == attn_sha
+
+
+def test_sharing_modes_cut_measured_l2_to_sm_bytes_against_their_unicast_twins(records, analytic):
+    # Each sharing workload against the unicast workload that computes the same output:
+    # the measured reduction tracks the analytic one (1.5x for a 2x1 cluster sharing B,
+    # 2x for 2x2 multicast and for the pair with 4-CTA B multicast).
+    from dense_gemm_cluster_gb300.workloads import UNICAST_TWIN
+    for name, twin in UNICAST_TWIN.items():
+        measured = records[twin]["lts_bytes"] / records[name]["lts_bytes"]
+        expected = analytic[twin][1].l2_to_sm_operand_bytes / analytic[name][1].l2_to_sm_operand_bytes
+        assert expected >= 1.5
+        assert abs(measured / expected - 1.0) < 0.25, f"{name}: measured {measured:.2f}x, analytic {expected:.2f}x"
