@@ -31,6 +31,8 @@ struct BenchParams {
     uint64_t* cycles;
     uint64_t* ns;
     uint32_t* verify;
+    uint8_t* landed;             // optional: each CTA's last landed tile, as it sits in shared memory
+    int* origin;                 // optional: that tile's (x, y) origin per CTA
     unsigned long long timeout_ns;
 };
 
@@ -166,6 +168,10 @@ tma_bench_kernel(const __grid_constant__ CUtensorMap tm, const BenchParams p) {
             const bool check = (it & 63) == 0 || it == total - 1;
             int x = 0, y = 0;
             if (check) tw.origin(p, x, y);
+            if (it == total - 1 && p.origin) {
+                p.origin[2 * blockIdx.x] = x;
+                p.origin[2 * blockIdx.x + 1] = y;
+            }
             const uint8_t* box = smem + slot * box_bytes;
             const int rs[2] = {0, p.box_rows - 1};
             const int js[2] = {0, 63};
@@ -197,6 +203,14 @@ tma_bench_kernel(const __grid_constant__ CUtensorMap tm, const BenchParams p) {
         p.verify[blockIdx.x] = ok ? bad : 0xFFFFFFFFu;
     }
     __syncthreads();
+    if (warp == 1 && p.landed && total > 0) {
+        // After the timed loop every load has landed and no more are issued: copy the
+        // last slot out whole, for a check of every element on the host.
+        const int last = (total - 1) % S;
+        const uint4* from = reinterpret_cast<const uint4*>(smem + last * box_bytes);
+        uint4* to = reinterpret_cast<uint4*>(p.landed + (size_t)blockIdx.x * box_bytes);
+        for (uint32_t i = lane; i < box_bytes / 16; i += 32) to[i] = from[i];
+    }
     cluster_sync();
 }
 
@@ -300,6 +314,8 @@ extern "C" gemm_status_t tma_bench_run(const tma_bench_options_t* opt, const voi
     p.cycles = cycles;
     p.ns = ns;
     p.verify = verify;
+    p.landed = static_cast<uint8_t*>(o.landed);
+    p.origin = o.origin;
     p.timeout_ns = o.wait_timeout_ns ? o.wait_timeout_ns : 2000000000ull;
     void* args[] = {&tm, &p};
     e = cudaLaunchKernelExC(&cfg, fn, args);

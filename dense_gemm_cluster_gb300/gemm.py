@@ -306,7 +306,7 @@ TMA_BENCH_MULTICAST_SLICED = 2
 class tma_bench_options_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "mode", "cluster", "ctas", "box_rows", "stages", "iters", "warmup", "streaming_stride")] + [
-        ("wait_timeout_ns", ctypes.c_uint64)]
+        ("wait_timeout_ns", ctypes.c_uint64), ("landed", ctypes.c_void_p), ("origin", ctypes.c_void_p)]
 
 
 _lib.tma_bench_run.argtypes = [ctypes.POINTER(tma_bench_options_t), _vp, _i64, _i64, _i64, _vp, _vp, _vp,

@@ -20,7 +20,10 @@ MODES = {"unicast": 0, "multicast": 1, "multicast_sliced": 2}
 
 
 def run(mode="unicast", cluster=2, box_rows=128, stages=4, iters=5000, warmup=50, stride=0, ctas=0,
-        rows=4096, cols=4096, src=None, device=0):
+        rows=4096, cols=4096, src=None, device=0, landed=False):
+    """One benchmark launch. With landed=True the result also holds every CTA's last landed
+    tile (uint8 array, ctas x box_rows x 128 bytes, swizzled as in shared memory) and its
+    (x, y) origin in src (int array, ctas x 2), for a full check against src."""
     import torch
     from . import gemm
     dev = torch.device("cuda", device)
@@ -33,6 +36,10 @@ def run(mode="unicast", cluster=2, box_rows=128, stages=4, iters=5000, warmup=50
     cycles = torch.zeros(nmax, dtype=torch.int64, device=dev)
     ns = torch.zeros(nmax, dtype=torch.int64, device=dev)
     verify = torch.zeros(nmax, dtype=torch.int32, device=dev)
+    if landed:
+        land = torch.zeros(nmax * box_rows * 128, dtype=torch.uint8, device=dev)
+        orig = torch.full((nmax * 2,), -1, dtype=torch.int32, device=dev)
+        o.landed, o.origin = land.data_ptr(), orig.data_ptr()
     stream = torch.cuda.current_stream(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -48,7 +55,11 @@ def run(mode="unicast", cluster=2, box_rows=128, stages=4, iters=5000, warmup=50
     nss = ns[:n].cpu().tolist()
     bad = verify[:n].cpu().tolist()
     per_cta_bytes = iters * box_rows * 128
-    return {
+    extra = {}
+    if landed:
+        extra = {"landed": land[:n * box_rows * 128].cpu().numpy().reshape(n, box_rows * 128),
+                 "origin": orig[:2 * n].cpu().numpy().reshape(n, 2)}
+    return {**extra,
         "mode": mode if cluster > 1 else "unicast", "cluster": cluster, "ctas": n, "box_rows": box_rows,
         "stages": stages, "iters": iters, "stride": stride, "kernel_ms": ms,
         "timed_ms_max": max(nss) / 1e6, "delivered_bytes": delivered, "issued_bytes": issued,

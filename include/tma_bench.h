@@ -45,6 +45,11 @@ typedef struct {
                              s > 0: iteration i loads tile (i*s*clusters + cluster id) mod tiles */
     uint64_t wait_timeout_ns; /* bound on every in-kernel wait, counted as 2 SM cycles per ns
                                  (this long at 2 GHz, longer at lower clocks); 0 = 2 s */
+    void *landed;         /* NULL, or a device array of ctas x box_rows x 128 bytes: after the timed
+                             loads each CTA copies its last landed tile there exactly as it sits in
+                             shared memory (128-byte swizzle: element (r, j) at byte
+                             r*128 + ((j/8) ^ (r%8))*16 + (j%8)*2), for a check of every element */
+    int *origin;          /* NULL, or a device array of 2 x ctas ints: that tile's (x, y) origin in src */
 } tma_bench_options_t;
 
 /* Runs the benchmark on `stream` (asynchronous) over a rows x cols bf16 matrix
