@@ -207,6 +207,17 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
         p.l2_hint_a = dgc::L2_HINT_EVICT_LAST;
         p.l2_hint_b = dgc::L2_HINT_EVICT_FIRST;
     }
+    // Serpentine k walk: in the raster band a cluster's next whole tile reuses its A
+    // rows a wave later, after the whole K range of a wave's operands has passed
+    // through L2. Walking k backwards on every other tile starts it on the k-blocks
+    // read last. Only for long K (at least 16 k-blocks) and at least two waves of
+    // whole tiles, where those re-reads come from DRAM (8192^3 pair + 4-CTA
+    // multicast: DRAM 1.41 -> 1.25 GB per launch, 588 -> 582 us; 4096^3 pair 79.1 -> 77.9 us;
+    // neither slower anywhere measured). A reversed tile sums
+    // its k-blocks in the other order, so it rounds differently from the same tile of
+    // a launch that walks it forwards.
+    p.k_serpentine = (p.l2_hint_a == dgc::L2_HINT_NONE && ceil_div(K, BK) >= 16 && clusters > 0 &&
+                      p.tiles >= 2 * clusters) ? 1 : 0;
     return GEMM_OK;
 }
 
@@ -619,6 +630,7 @@ gemm_status_t dgc_host::run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t 
     kp.a_l2 = pl.l2_hint_a;
     kp.b_l2 = pl.l2_hint_b;
     kp.k_rotate = pl.k_rotate;
+    kp.k_serpentine = pl.k_serpentine;
     // Prefetch each CTA's first stages into L2 before waiting for the previous grid:
     // back to back, a launch's DRAM fill overlaps its predecessor's last tiles (measured
     // 16384 x 128 x 8192: 48.5 -> 47.2 us; 4096^3: 90.3 -> 89.2 us; 8192^3 unchanged).

@@ -41,8 +41,11 @@
 // L2 traffic: when the tile grid is one tile wide, the operand that each tile
 // reads alone is loaded with an evict-first policy and the one every tile reads
 // with evict-last (K-major streamed rows also start at a tile-dependent k-block);
-// each producer prefetches its first stages into L2 before waiting for the
-// previous grid in the stream (programmatic dependent launch).
+// on long-K grids of several waves a cluster's successive whole tiles, which share
+// their A rows in the raster band, walk k in alternating directions, so each
+// starts on the k-blocks L2 received last; each producer prefetches its first
+// stages into L2 before waiting for the previous grid in the stream
+// (programmatic dependent launch).
 //
 // Every wait is bounded by wait_timeout_ns of %globaltimer; on expiry the
 // thread records a status word in global memory, raises a CTA-wide abort flag
@@ -107,6 +110,7 @@ struct KernelParams {
     int a_shared, b_shared;  // 1: one matrix serves every product of the batch (stride 0)
     int a_l2, b_l2;          // L2 eviction priority of the operand's loads: 0 none, 1 evict first, 2 evict last
     int k_rotate;            // 1: whole tiles start their k walk at a tile-dependent k-block
+    int k_serpentine;        // 1: a cluster's successive whole tiles alternate their k direction
     int prefetch;            // 1: prefetch the first stages into L2 before waiting for the previous grid
 };
 
@@ -354,10 +358,10 @@ struct OperandPlan {
     int shared;            // one matrix for the whole batch: batch coordinate 0
 };
 
-template <int G, int BK>
+template <int G, int BK, bool HINT>
 __device__ __forceinline__ void tma_issue(const OperandPlan& op, bool mcast, uint32_t dst, uint32_t bar, int x, int y,
-                                          int z, int w, bool four_d, bool hint, uint64_t pol) {
-    if (hint) {
+                                          int z, int w, bool four_d, uint64_t pol) {
+    if constexpr (HINT) {
         if (four_d) {
             if (G == 1) {
                 if (mcast) tma_load_4d_mcast_hint(dst, op.tmap, bar, x, y, z, w, (uint16_t)op.mask, pol);
@@ -375,8 +379,7 @@ __device__ __forceinline__ void tma_issue(const OperandPlan& op, bool mcast, uin
                 else       tma_load_3d_pair_hint(dst, op.tmap, bar, x, y, z, pol);
             }
         }
-        return;
-    }
+    } else {
     if (four_d) {
         if (G == 1) {
             if (mcast) tma_load_4d_mcast(dst, op.tmap, bar, x, y, z, w, (uint16_t)op.mask);
@@ -393,6 +396,7 @@ __device__ __forceinline__ void tma_issue(const OperandPlan& op, bool mcast, uin
             if (mcast) tma_load_3d_pair_mcast(dst, op.tmap, bar, x, y, z, (uint16_t)op.mask);
             else       tma_load_3d_pair(dst, op.tmap, bar, x, y, z);
         }
+    }
     }
 }
 
@@ -458,7 +462,13 @@ __device__ __forceinline__ void prefetch_first_stages(const KernelParams& p, con
     }
 }
 
-template <int G, int BK>
+// WALK_PLAIN: k-blocks in order, no hints. WALK_ONE_WIDE: the planner's one-tile-wide
+// grid policy (L2 eviction priorities and, when set, the rotated k walk). WALK_SERPENTINE:
+// whole tiles alternate their k direction from one of a cluster's tiles to the next, so
+// each starts on the k-blocks its predecessor read last.
+enum : int { WALK_PLAIN = 0, WALK_ONE_WIDE = 1, WALK_SERPENTINE = 2 };
+
+template <int G, int BK, int WALK>
 __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan& op, bool is_a, uint32_t full0,
                                         uint32_t empty0, uint32_t rank, uint32_t leader, int cx, int cy, int rx,
                                         int ry, int BNv, int BN_CTAv, volatile int* abort_flag,
@@ -478,10 +488,12 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
     const SliceGeom sg = slice_geom<BK>(op);
     bool extra_tx = is_a && (p.debug_flags & 1) != 0;
     // L2 eviction priority of this operand's loads (chosen by the planner).
-    const int l2 = is_a ? p.a_l2 : p.b_l2;
-    const bool hint = l2 != L2_HINT_NONE;
-    const uint64_t pol = l2 == L2_HINT_EVICT_FIRST ? l2_policy_evict_first()
-                       : l2 == L2_HINT_EVICT_LAST  ? l2_policy_evict_last() : 0ull;
+    constexpr bool HINTED = WALK == WALK_ONE_WIDE;
+    uint64_t pol = 0;
+    if constexpr (HINTED) {
+        const int l2 = is_a ? p.a_l2 : p.b_l2;
+        pol = l2 == L2_HINT_EVICT_FIRST ? l2_policy_evict_first() : l2_policy_evict_last();
+    }
     int stage = 0;
     uint32_t phase = 0;
     WorkIter wi;
@@ -508,9 +520,12 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
         const int mn0 = is_a ? (tc.ctm * cx + rx) * BLOCK_M
                              : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
         const int nkb = w.kb1 - w.kb0;
-        const int rot = k_rotation(p, w);
+        const int rot = WALK == WALK_ONE_WIDE ? k_rotation(p, w) : 0;
+        const bool back = WALK == WALK_SERPENTINE && w.kind == WORK_WHOLE && ((w.tile / clusters) & 1);
         for (int i = 0; i < nkb; ++i) {
-            const int kb = w.kb0 + (i + rot < nkb ? i + rot : i + rot - nkb);
+            const int kb = WALK == WALK_ONE_WIDE ? w.kb0 + (i + rot < nkb ? i + rot : i + rot - nkb)
+                         : WALK == WALK_SERPENTINE ? (back ? w.kb1 - 1 - i : w.kb0 + i)
+                                                   : w.kb0 + i;
             if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, p, abort_flag, ERR_WAIT_EMPTY, (uint32_t)stage, t))
                 return false;
 #pragma unroll
@@ -528,12 +543,12 @@ __device__ __forceinline__ bool produce(const KernelParams& p, const OperandPlan
             if (op.mn_major) {
                 const int y = kb * BK + op.slice * sg.k_rows;
                 for (int box = 0; box < op.rows / 64; ++box)
-                    tma_issue<G, BK>(op, mcast, dst + (uint32_t)(box * BK * 128), bar, mn0 + box * 64, y, zb, 0,
-                                     false, hint, pol);
+                    tma_issue<G, BK, HINTED>(op, mcast, dst + (uint32_t)(box * BK * 128), bar, mn0 + box * 64, y, zb,
+                                             0, false, pol);
             } else if (op.kmap4) {
-                tma_issue<G, BK>(op, mcast, dst, bar, 0, mn0 + sg.r0, kb * NAT + sg.atom0, zb, true, hint, pol);
+                tma_issue<G, BK, HINTED>(op, mcast, dst, bar, 0, mn0 + sg.r0, kb * NAT + sg.atom0, zb, true, pol);
             } else {
-                tma_issue<G, BK>(op, mcast, dst, bar, kb * BK, mn0 + sg.r0, zb, 0, false, hint, pol);
+                tma_issue<G, BK, HINTED>(op, mcast, dst, bar, kb * BK, mn0 + sg.r0, zb, 0, false, pol);
             }
             if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -849,14 +864,16 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const long long cluster = cluster_id_x();
     const long long clusters = num_clusters_x();
     // The producers' operand plans (A: warp 0, B: warp 6).
-    OperandPlan op;
-    if (warp == 0) op = OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, p.a_kmap4, idxA, gA, maskA,
-                                    p.a_shared};
-    else           op = OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB,
-                                    p.b_shared};
+    auto operand_plan = [&](bool is_a) -> OperandPlan {
+        return is_a ? OperandPlan{&tmA, smem_u32(sA), A_BYTES, BLOCK_M, p.a_mn_major, p.a_kmap4, idxA, gA, maskA,
+                                  p.a_shared}
+                    : OperandPlan{&tmB, smem_u32(sB), B_BYTES, BN_CTA, p.b_mn_major, p.b_kmap4, idxB, gB, maskB,
+                                  p.b_shared};
+    };
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (p.prefetch && (warp == 0 || warp == 6) && lane == 0)
-        prefetch_first_stages<G, BK>(p, op, warp == 0, cx, cy, rx, ry, BN, BN_CTA, cluster, clusters, S);
+        prefetch_first_stages<G, BK>(p, operand_plan(warp == 0), warp == 0, cx, cy, rx, ry, BN, BN_CTA, cluster,
+                                     clusters, S);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     ClcCtx clc_ctx;
@@ -872,9 +889,20 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // ------------------------------------------------------------ producers (A: warp 0, B: warp 6)
         if (lane == 0) {
             const bool is_a = warp == 0;
-            prefetch_tmap(is_a ? static_cast<const void*>(&tmA) : static_cast<const void*>(&tmB));
-            produce<G, BK>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank, leader, cx, cy, rx, ry,
-                       BN, BN_CTA, abort_flag, cluster, clusters, S, &clc_ctx, smem_u32(&ring_empty[0]));
+            const OperandPlan op = operand_plan(is_a);
+            prefetch_tmap(op.tmap);
+            if (p.a_l2 != L2_HINT_NONE)
+                produce<G, BK, WALK_ONE_WIDE>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank,
+                                              leader, cx, cy, rx, ry, BN, BN_CTA, abort_flag, cluster, clusters, S,
+                                              &clc_ctx, smem_u32(&ring_empty[0]));
+            else if (p.k_serpentine)
+                produce<G, BK, WALK_SERPENTINE>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank,
+                                                leader, cx, cy, rx, ry, BN, BN_CTA, abort_flag, cluster, clusters, S,
+                                                &clc_ctx, smem_u32(&ring_empty[0]));
+            else
+                produce<G, BK, WALK_PLAIN>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank,
+                                           leader, cx, cy, rx, ry, BN, BN_CTA, abort_flag, cluster, clusters, S,
+                                           &clc_ctx, smem_u32(&ring_empty[0]));
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer

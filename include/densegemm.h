@@ -142,6 +142,8 @@ typedef struct {
                                  tile of it is read by one cluster tile only), 2 evict last (read
                                  by every cluster tile) */
     int k_rotate;             /* 1: whole tiles start their k walk at a tile-dependent k-block */
+    int k_serpentine;         /* 1: a cluster's successive whole tiles walk k in alternating directions
+                                 (long K, at least two waves of whole tiles) */
 } gemm_plan_t;
 
 /* Default options: unicast, 1x1 cluster, cta_group 1, A row-major, B column-major,

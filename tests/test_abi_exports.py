@@ -288,3 +288,16 @@ def test_plan_l2_hints_and_k_rotation(lib):
         assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (0, 0, 0), args
     s, p = plan(lib, 4096, 4096, 128, batch=128, layout_b="col", cluster_m=4, mode="mcast", mcast_b=1)
     assert s == 0 and (p.l2_hint_a, p.l2_hint_b, p.k_rotate) == (0, 0, 0)
+
+
+def test_plan_serpentine_k_walk(lib):
+    # Long K and at least two waves of whole tiles: successive tiles alternate direction.
+    s, p = plan(lib, 8192, 8192, 8192, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1)
+    assert s == 0 and p.k_serpentine == 1 and p.k_rotate == 0
+    # Short K (the score form's 2 k-blocks; 5 k-blocks), one wave, or a one-tile-wide grid: in order.
+    for args, kw in [((4096, 4096, 128), dict(batch=128, layout_b="col", cluster_m=4, mode="mcast", mcast_b=1)),
+                     ((3072, 4096, 320), dict()),
+                     ((1024, 1024, 8192), dict()),
+                     ((16384, 128, 8192), dict(cta_group=2, cluster_m=4, mode="mcast", mcast_b=1, block_n=128))]:
+        s, p = plan(lib, *args, **kw)
+        assert s == 0 and p.k_serpentine == 0, args
