@@ -98,6 +98,20 @@ def test_rotated_k_walk_with_l2_hints_matches_oracle(G, opts):
     assert_close(got, p.reference(), p.K, "f32", f"rotated k walk {opts}")
 
 
+@pytest.mark.parametrize("opts", [dict(max_clusters=20, schedule="dp"),
+                                  dict(max_clusters=20, schedule="stream_k"),
+                                  dict(cta_group=2, cluster_m=4, mode="mcast", mcast_b=1, max_clusters=6)])
+def test_serpentine_k_walk_matches_oracle(G, opts):
+    # Long K on several waves of whole tiles: every other whole tile of a cluster walks its
+    # k-blocks backwards, so it starts on the partial last k-block (K = 1100 is 17.2 blocks
+    # of 64). With stream-K the last waves' split pieces stay in order.
+    p = Problem(2048, 1536, 1100, la="row", lb="col", out="bf16", beta=0.5, seed=98)
+    s, plan = G.gemm_plan(G.make_options(**options_for(p, **opts)), p.M, p.N, p.K, 1, 152)
+    assert s == 0 and plan.k_serpentine == 1 and plan.tiles >= 2 * plan.clusters
+    got = _run(G, p, 1.0, 0.5, **opts)
+    assert_close(got, p.reference(1.0, 0.5), p.K, "bf16", f"serpentine {opts}")
+
+
 @pytest.mark.parametrize("lb", ["row", "col"])
 def test_multicast_mn_major_operands(G, lb):
     p = Problem(520, 700, 256, la="col", lb=lb, out="f32", seed=6)
