@@ -132,6 +132,9 @@ __host__ __device__ __forceinline__ TileCoord tile_coord(const KernelParams& p, 
     const int local = (int)(r - (long long)group * in_group);
     c.ctm = first_m + local % gsz;
     c.ctn = local / gsz;
+    // With the serpentine walk the bands snake too: odd bands walk their columns from the
+    // last, so a band starts on the B columns the previous band read last.
+    if (p.k_serpentine && (group & 1)) c.ctn = p.tiles_n - 1 - c.ctn;
     return c;
 }
 

@@ -143,7 +143,8 @@ typedef struct {
                                  by every cluster tile) */
     int k_rotate;             /* 1: whole tiles start their k walk at a tile-dependent k-block */
     int k_serpentine;         /* 1: a cluster's successive whole tiles walk k in alternating directions
-                                 (long K, at least two waves of whole tiles) */
+                                 and odd raster bands walk their columns from the last (long K, at
+                                 least two waves of whole tiles) */
 } gemm_plan_t;
 
 /* Default options: unicast, 1x1 cluster, cta_group 1, A row-major, B column-major,

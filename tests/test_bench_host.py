@@ -74,3 +74,50 @@ def test_reference_arm_prints_one_contract_line_without_a_gpu():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_l2_to_sm_report_divides_the_unicast_twins_measured_bytes():
+    # The bench line's multicast evidence: the unicast twin's ncu L2 -> SM bytes over this
+    # workload's, both from records taken on the current kernel sources.
+    import bench
+    from dense_gemm_cluster_gb300 import build
+    build.build()
+    from dense_gemm_cluster_gb300 import gemm
+    from dense_gemm_cluster_gb300.workloads import WORKLOADS
+    w = WORKLOADS["gemm8192_bf16_pair_mcastB4"]
+    opts = gemm.make_options(layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out,
+                             **w.options)
+    _, plan = gemm.gemm_plan(opts, w.M, w.N, w.K, w.batch, 152)
+    _, uni = gemm.gemm_plan(gemm.make_options(layout_a=w.layout_a, layout_b=w.layout_b, block_n=256),
+                            w.M, w.N, w.K, w.batch, 152)
+    rec = bench.recorded_traffic(w.name)
+    r = bench.l2_to_sm_report(w, plan, uni, rec)
+    assert r["unicast_workload"] == "gemm8192_bf16_unicast"
+    assert r["reduction_vs_unicast"] == pytest.approx(2.0)
+    twin = bench.recorded_traffic("gemm8192_bf16_unicast")
+    assert r["reduction_measured"] == pytest.approx(twin["lts_bytes"] / rec["lts_bytes"])
+    assert r["reduction_measured"] >= 1.8
+    # without a record (stale or missing) nothing is claimed
+    r = bench.l2_to_sm_report(w, plan, uni, None)
+    assert r["measured"] is None and r["reduction_measured"] is None
+    # a workload without a unicast twin reports the analytic ratio only
+    s = WORKLOADS["scores_8x16x4096x4096x128"]
+    r = bench.l2_to_sm_report(s, plan, uni, bench.recorded_traffic(s.name))
+    assert r["unicast_workload"] is None and r["reduction_measured"] is None
+
+
+def test_nvml_clock_summary_windows_and_reasons():
+    # The in-process clock record: only samples inside the window count; the clock-event
+    # reason bits decode to the names the throttle checks use.
+    import bench
+    c = bench.NvmlClocks.__new__(bench.NvmlClocks)
+    c.ok, c.max_mhz, c.period_s = True, 2070.0, 0.001
+    c.samples = [(0.5, 2070.0, 150.0, 0x0),                 # before the window
+                 (1.0, 2070.0, 900.0, 0x0), (1.1, 1500.0, 1390.0, 0x4),
+                 (1.2, 1480.0, 1395.0, 0x4 | 0x40), (2.5, 900.0, 100.0, 0x8)]   # the last after it
+    s = c.summary(0.9, 1.3)
+    assert s["samples"] == 3 and s["sm_mhz"] == 1500.0 and s["sm_mhz_min"] == 1480.0
+    assert s["power_w_max"] == 1395.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    c.ok = False
+    assert c.summary(0.0, 9.0)["reasons"] == ["nvml unavailable"]
