@@ -510,8 +510,12 @@ def bench_ours(args, w: Workload):
 
     opts = dict(w.options)
     if world > 1:
-        # cluster multicast stays off when several GPUs take part
+        # Cluster multicast stays off when several GPUs take part. Without it a pair kernel
+        # gains nothing from clusters of more than one pair (4-CTA clusters only leave SMs
+        # idle: 36 fit on 152 SMs), so the pairs run in 2-CTA clusters.
         opts["mode"] = "unicast"
+        if opts.get("cta_group", 1) == 2 and opts.get("cluster_m", 1) > 2 and opts.get("cluster_n", 1) == 1:
+            opts["cluster_m"] = 2
     g = gemm.Gemm(local, layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out, **opts)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     s, plan = gemm.gemm_plan(g.options, w.M, w.N, w.K, w.batch, sms)
