@@ -5,7 +5,7 @@ cta_group 1 here (unicast and cluster multicast); the pair MMA has its own file.
 import numpy as np
 import pytest
 
-from gpu_cases import Problem, assert_close, decode, options_for
+from gpu_cases import Problem, assert_close, decode, options_for, torch_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -110,6 +110,40 @@ def test_serpentine_k_walk_matches_oracle(G, opts):
     assert s == 0 and plan.k_serpentine == 1 and plan.tiles >= 2 * plan.clusters
     got = _run(G, p, 1.0, 0.5, **opts)
     assert_close(got, p.reference(1.0, 0.5), p.K, "bf16", f"serpentine {opts}")
+
+
+def test_serpentine_walk_and_snaking_bands_over_a_batch(G):
+    # Three products of 1024 x 1280 x 2048 on 8 clusters: 32 k-blocks, several waves of whole
+    # tiles per product, bands of 4 tile rows that snake within each product.
+    import torch
+    M, N, K, batch = 1024, 1280, 2048, 3
+    s, plan = G.gemm_plan(G.make_options(layout_a="row", layout_b="col", out_type="f32", max_clusters=8),
+                          M, N, K, batch, 152)
+    assert s == 0 and plan.k_serpentine == 1
+    probs = [Problem(M, N, K, la="row", lb="col", out="f32", seed=70 + i) for i in range(batch)]
+    dA = torch.cat([torch_dev(p.A).view(-1) for p in probs])
+    dB = torch.cat([torch_dev(p.B).view(-1) for p in probs])
+    dC = torch.full((batch * M * N,), float("nan"), dtype=torch.float32, device="cuda")
+    g = G.Gemm(0, layout_a="row", layout_b="col", layout_c="row", out_type="f32", max_clusters=8)
+    try:
+        g.run_strided_batched(M, N, K, dA, probs[0].lda, M * probs[0].lda, dB, probs[0].ldb, N * probs[0].ldb,
+                              dC, N, M * N, batch)
+        assert g.query_status() == G.GEMM_OK
+    finally:
+        g.close()
+    out = dC.cpu().numpy().astype(np.float64).reshape(batch, M, N)
+    for i, p in enumerate(probs):
+        assert_close(out[i], p.reference(), K, "f32", f"batch {i}")
+
+
+def test_one_tile_wide_hints_through_a_column_major_c(G):
+    # C column-major runs C^T = B^T A^T: a 1536 x 100 C becomes a launched 100 x 1536 grid one
+    # tile tall, so the launched B (= A^T) streams evict-first and A (= B^T) stays evict-last.
+    p = Problem(1536, 100, 1000, la="row", lb="row", lc="col", out="bf16", beta=0.5, seed=99)
+    s, plan = G.gemm_plan(G.make_options(**options_for(p, block_n=128)), p.M, p.N, p.K, 1, 152)
+    assert s == 0 and plan.transposed == 1 and (plan.l2_hint_a, plan.l2_hint_b) == (2, 1)
+    got = _run(G, p, 1.0, 0.5, block_n=128)
+    assert_close(got, p.reference(1.0, 0.5), p.K, "bf16", "one tile wide, column-major C")
 
 
 @pytest.mark.parametrize("lb", ["row", "col"])
