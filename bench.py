@@ -196,7 +196,7 @@ class NvmlClocks:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device, period_s: float = 0.001):
+    def __init__(self, device, period_s: float = 0.0005):
         import ctypes
         import threading
         self.period_s = period_s
