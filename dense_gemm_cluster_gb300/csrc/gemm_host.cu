@@ -220,6 +220,16 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     // a launch that walks it forwards.
     p.k_serpentine = (p.l2_hint_a == dgc::L2_HINT_NONE && ceil_div(K, BK) >= 16 && clusters > 0 &&
                       p.tiles >= 2 * clusters) ? 1 : 0;
+    // Each producer prefetches the first k-blocks of its first tile into L2 before
+    // waiting for the previous grid: back to back, a launch's first DRAM reads overlap
+    // its predecessor's last tiles. A ring's worth in general (16384 x 128 x 8192:
+    // 48.5 -> 47.2 us; 4096^3: 90.3 -> 89.2 us; deeper was 0.5 % slower there; 8192^3
+    // and the attention-score batch unchanged); three rings' worth where the grid is one
+    // tile wide and each tile streams its own operand (16384 x 128 x 8192: 48.1 -> 46.8
+    // us, 128 x 16384 x 8192: 46.4 -> 45.9 us; four rings and more crowd L2 and slow both).
+    // None with cluster launch control, which launches without programmatic dependent
+    // launch.
+    p.prefetch_kb = o.schedule == 3 ? 0 : (p.l2_hint_a != dgc::L2_HINT_NONE ? 3 : 1) * S;
     return GEMM_OK;
 }
 
@@ -633,11 +643,7 @@ gemm_status_t dgc_host::run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t 
     kp.b_l2 = pl.l2_hint_b;
     kp.k_rotate = pl.k_rotate;
     kp.k_serpentine = pl.k_serpentine;
-    // Prefetch each CTA's first stages into L2 before waiting for the previous grid:
-    // back to back, a launch's DRAM fill overlaps its predecessor's last tiles (measured
-    // 16384 x 128 x 8192: 48.5 -> 47.2 us; 4096^3: 90.3 -> 89.2 us; 8192^3 unchanged).
-    // Cluster launch control launches without programmatic dependent launch.
-    kp.prefetch = o.schedule == 3 ? 0 : 1;
+    kp.prefetch_kb = pl.prefetch_kb;
 
     void* fn = pick_kernel(BN, G, BK);
     const int bi = BN == 256 ? 1 : 0, gi = G - 1, ki = BK == 128 ? 1 : 0;

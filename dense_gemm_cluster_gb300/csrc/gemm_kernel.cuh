@@ -43,9 +43,9 @@
 // with evict-last (K-major streamed rows also start at a tile-dependent k-block);
 // on long-K grids of several waves a cluster's successive whole tiles, which share
 // their A rows in the raster band, walk k in alternating directions, so each
-// starts on the k-blocks L2 received last; each producer prefetches its first
-// stages into L2 before waiting for the previous grid in the stream
-// (programmatic dependent launch).
+// starts on the k-blocks L2 received last; each producer prefetches the first
+// k-blocks of its first tile into L2 before waiting for the previous grid in the
+// stream (programmatic dependent launch), deeper than the ring on one-tile-wide grids.
 //
 // Every wait is bounded by wait_timeout_ns of %globaltimer; on expiry the
 // thread records a status word in global memory, raises a CTA-wide abort flag
@@ -111,7 +111,7 @@ struct KernelParams {
     int a_l2, b_l2;          // L2 eviction priority of the operand's loads: 0 none, 1 evict first, 2 evict last
     int k_rotate;            // 1: whole tiles start their k walk at a tile-dependent k-block
     int k_serpentine;        // 1: a cluster's successive whole tiles alternate their k direction
-    int prefetch;            // 1: prefetch the first stages into L2 before waiting for the previous grid
+    int prefetch_kb;         // k-blocks of the first tile prefetched into L2 before waiting for the previous grid
 };
 
 enum : int { L2_HINT_NONE = 0, L2_HINT_EVICT_FIRST = 1, L2_HINT_EVICT_LAST = 2 };
@@ -432,14 +432,14 @@ __device__ __forceinline__ SliceGeom slice_geom(const OperandPlan& op) {
     return g;
 }
 
-// Prefetches into L2 this issuer's part of the first stages of its cluster's first
-// work item: the same boxes produce() will load, so a launch that follows another in
+// Prefetches into L2 this issuer's part of the first `nkb_max` k-blocks of its cluster's
+// first work item: the same boxes produce() will load, so a launch that follows another in
 // the stream overlaps its first DRAM reads with the previous grid's last tiles. A
 // prefetch returns no data to the SM, so it may run before griddepcontrol.wait.
 template <int G, int BK>
 __device__ __forceinline__ void prefetch_first_stages(const KernelParams& p, const OperandPlan& op, bool is_a, int cx,
                                                       int cy, int rx, int ry, int BNv, int BN_CTAv, long long cluster,
-                                                      long long clusters, int S) {
+                                                      long long clusters, int nkb_max) {
     constexpr int NAT = BK / ATOM_K;
     WorkIter wi;
     wi.init(p, cluster, clusters, nullptr);
@@ -452,7 +452,7 @@ __device__ __forceinline__ void prefetch_first_stages(const KernelParams& p, con
                          : (tc.ctn * cy + ry) * BNv + (G == 2 ? (rx & 1) * BN_CTAv : 0);
     const int nkb = w.kb1 - w.kb0;
     const int rot = k_rotation(p, w);
-    for (int i = 0; i < S && i < nkb; ++i) {
+    for (int i = 0; i < nkb_max && i < nkb; ++i) {
         const int kb = w.kb0 + (i + rot < nkb ? i + rot : i + rot - nkb);
         if (op.mn_major) {
             const int y = kb * BK + op.slice * sg.k_rows;
@@ -874,9 +874,9 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                   p.b_shared};
     };
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (p.prefetch && (warp == 0 || warp == 6) && lane == 0)
+    if (p.prefetch_kb > 0 && (warp == 0 || warp == 6) && lane == 0)
         prefetch_first_stages<G, BK>(p, operand_plan(warp == 0), warp == 0, cx, cy, rx, ry, BN, BN_CTA, cluster,
-                                     clusters, S);
+                                     clusters, p.prefetch_kb);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     ClcCtx clc_ctx;

@@ -52,7 +52,7 @@ class gemm_plan_t(ctypes.Structure):
         "group_a", "group_b", "transposed")] + [
         ("tiles", ctypes.c_int64), ("clusters", ctypes.c_int64), ("l2_to_sm_operand_bytes", ctypes.c_int64),
         ("stream_k_tiles", ctypes.c_int64), ("l2_hint_a", ctypes.c_int), ("l2_hint_b", ctypes.c_int),
-        ("k_rotate", ctypes.c_int), ("k_serpentine", ctypes.c_int)]
+        ("k_rotate", ctypes.c_int), ("k_serpentine", ctypes.c_int), ("prefetch_kb", ctypes.c_int)]
 
 
 _i64, _i32, _f32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p

@@ -145,6 +145,9 @@ typedef struct {
     int k_serpentine;         /* 1: a cluster's successive whole tiles walk k in alternating directions
                                  and odd raster bands walk their columns from the last (long K, at
                                  least two waves of whole tiles) */
+    int prefetch_kb;          /* k-blocks of its first tile each producer prefetches into L2 before
+                                 waiting for the previous grid in the stream: the stage count, three
+                                 times it on one-tile-wide grids, 0 with cluster launch control */
 } gemm_plan_t;
 
 /* Default options: unicast, 1x1 cluster, cta_group 1, A row-major, B column-major,

@@ -301,3 +301,19 @@ def test_plan_serpentine_k_walk(lib):
                      ((16384, 128, 8192), dict(cta_group=2, cluster_m=4, mode="mcast", mcast_b=1, block_n=128))]:
         s, p = plan(lib, *args, **kw)
         assert s == 0 and p.k_serpentine == 0, args
+
+
+def test_plan_l2_prefetch_depth(lib):
+    # A ring's worth of k-blocks in general; three on one-tile-wide grids, where each
+    # tile streams an operand of its own; none with cluster launch control.
+    s, p = plan(lib, 8192, 8192, 8192, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1)
+    assert s == 0 and p.prefetch_kb == p.stages
+    s, p = plan(lib, 4096, 4096, 128, batch=128, layout_b="col", cluster_m=4, mode="mcast", mcast_b=1)
+    assert s == 0 and p.prefetch_kb == p.stages
+    for args, kw in [((16384, 128, 8192), dict(layout_b="row", cta_group=2, cluster_m=4, block_n=128, mode="mcast",
+                                               mcast_b=1)),
+                     ((128, 16384, 8192), dict(layout_b="row", cluster_n=2, block_n=128, mode="mcast", mcast_a=1))]:
+        s, p = plan(lib, *args, **kw)
+        assert s == 0 and p.l2_hint_a != 0 and p.prefetch_kb == 3 * p.stages, args
+    s, p = plan(lib, 8192, 8192, 8192, schedule="clc")
+    assert s == 0 and p.prefetch_kb == 0
