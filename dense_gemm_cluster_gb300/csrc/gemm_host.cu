@@ -74,8 +74,8 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
         return fail(err, GEMM_ERR_INVALID_ARG, "layouts must be GEMM_ROW_MAJOR or GEMM_COL_MAJOR");
     if (o.out_type != GEMM_OUT_BF16 && o.out_type != GEMM_OUT_F32)
         return fail(err, GEMM_ERR_INVALID_ARG, "out_type must be GEMM_OUT_BF16 or GEMM_OUT_F32");
-    if (o.cta_group != 1 && o.cta_group != 2)
-        return fail(err, GEMM_ERR_UNSUPPORTED, "cta_group must be 1 or 2");
+    if (o.cta_group < 0 || o.cta_group > 2)
+        return fail(err, GEMM_ERR_UNSUPPORTED, "cta_group must be 0 (auto), 1 or 2");
     if (!pow2_le8(o.cluster_m) || !pow2_le8(o.cluster_n) || o.cluster_m * o.cluster_n > 8)
         return fail(err, GEMM_ERR_UNSUPPORTED, "cluster %dx%d: each extent 1/2/4/8 and at most 8 CTAs",
                     o.cluster_m, o.cluster_n);
@@ -98,7 +98,11 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
     const bool swap = o.layout_c == GEMM_COL_MAJOR;
     const int cm = swap ? o.cluster_n : o.cluster_m;
     const int cn = swap ? o.cluster_m : o.cluster_n;
-    const int G = o.cta_group;
+    // Auto: the pair MMA wherever the cluster's M extent is even. Each CTA then feeds
+    // its tensor core half of B's columns per k-step, which unloads the shared-memory
+    // port that bounds single-CTA tiles (4096^3 in 2x1 clusters: 1764 against 1556
+    // TFLOP/s with B multicast instead).
+    const int G = o.cta_group ? o.cta_group : ((cm & 1) ? 1 : 2);
     if (G == 2 && (cm & 1))
         return fail(err, GEMM_ERR_UNSUPPORTED,
                     "cta_group 2 pairs CTAs along M: the cluster extent along M%s must be even",

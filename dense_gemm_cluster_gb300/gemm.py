@@ -228,7 +228,8 @@ def make_options(**kw) -> gemm_options_t:
 
 class Gemm:
     """A handle bound to one device and one set of options (the fields of gemm_options_t as
-    keywords: mode, mcast_a, mcast_b, cluster_m, cluster_n, cta_group, layout_a/b/c ("row" or
+    keywords: mode, mcast_a, mcast_b, cluster_m, cluster_n, cta_group (1, 2, or 0 for the pair
+    wherever the cluster's extent along M is even), layout_a/b/c ("row" or
     "col"), out_type ("bf16" or "f32"), block_n, block_k, stages, max_clusters, group_m,
     schedule ("auto", "dp", "stream_k", "clc"), wait_timeout_ns, host_parts).
 

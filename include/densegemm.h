@@ -85,7 +85,9 @@ typedef struct {
                            (cluster_m of them, or cluster_m / 2 pairs with cta_group 2) */
     int cluster_m;      /* CTAs per cluster along M: 1, 2, 4 or 8 */
     int cluster_n;      /* CTAs per cluster along N: 1, 2, 4 or 8; cluster_m*cluster_n <= 8 */
-    int cta_group;      /* 1, or 2 for the pair MMA (cluster_m must then be even) */
+    int cta_group;      /* 1, 2 for the pair MMA (cluster_m must then be even), or 0: the
+                           pair wherever the cluster's extent along M is even (along N for
+                           column-major C), else 1; gemm_plan_t.cta_group reports the choice */
     int layout_a;       /* gemm_layout_t of A (M x K) */
     int layout_b;       /* gemm_layout_t of B (K x N) */
     int layout_c;       /* gemm_layout_t of C (M x N) */

@@ -87,7 +87,22 @@ def test_plan_column_major_c_swaps_roles(lib):
     assert (p.cluster_m, p.cluster_n) == (2, 1) and p.group_b == 2 and p.group_a == 1
 
 
+def test_plan_auto_cta_group_pairs_even_cluster_rows(lib):
+    # cta_group 0: the pair MMA wherever the cluster's extent along M is even, as launched
+    # (column-major C runs C^T, so there it is cluster_n that must be even).
+    for kw, want in [(dict(cluster_m=2), 2), (dict(cluster_m=4, mode="mcast", mcast_b=1), 2),
+                     (dict(cluster_m=2, cluster_n=2, mode="mcast", mcast_a=1), 2), (dict(), 1),
+                     (dict(cluster_n=2, mode="mcast", mcast_a=1), 1),
+                     (dict(cluster_n=2, layout_c="col"), 2), (dict(cluster_m=2, layout_c="col"), 1)]:
+        s, p = plan(lib, 4096, 4096, 4096, cta_group=0, **kw)
+        assert s == 0 and p.cta_group == want, kw
+    # The auto pair shares B within the pair: a 4-CTA cluster multicasts it across 2 pairs.
+    s, p = plan(lib, 4096, 4096, 4096, cta_group=0, cluster_m=4, mode="mcast", mcast_b=1)
+    assert s == 0 and p.group_b == 2
+
+
 @pytest.mark.parametrize("kw,code", [
+    (dict(cta_group=-1), 2),
     (dict(cta_group=3), 2),
     (dict(cluster_m=3), 2),
     (dict(cluster_m=4, cluster_n=4), 2),

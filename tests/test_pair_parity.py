@@ -110,3 +110,16 @@ def test_pair_sub_wave_problem_spreads_over_more_clusters(G):
     b = _run(G, p, 1.0, 0.5, cta_group=2, cluster_m=2)
     assert_close(a, p.reference(1.0, 0.5), 8192, "bf16", "pair sub-wave")
     assert np.array_equal(a, b)
+
+
+def test_auto_cta_group_picks_the_pair_and_matches_the_oracle(G):
+    # cta_group 0 with an even cluster extent along M runs the pair MMA: the same launch,
+    # bit for bit, as asking for cta_group 2, and within the tolerance of the oracle.
+    p = Problem(700, 1100, 448, la="row", lb="col", out="bf16", beta=0.5, seed=21)
+    s, plan = G.gemm_plan(G.make_options(**options_for(p, cta_group=0, cluster_m=4, mode="mcast", mcast_b=1)),
+                          p.M, p.N, p.K, 1, 152)
+    assert s == 0 and plan.cta_group == 2
+    auto = _run(G, p, 1.0, 0.5, cta_group=0, cluster_m=4, mode="mcast", mcast_b=1)
+    pair = _run(G, p, 1.0, 0.5, cta_group=2, cluster_m=4, mode="mcast", mcast_b=1)
+    assert np.array_equal(auto, pair)
+    assert_close(auto, p.reference(1.0, 0.5), 448, "bf16", "auto cta_group")
