@@ -106,6 +106,30 @@ def rated_tensor_peak(device, clocks) -> dict:
     return {"tflops": sms * RATED_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12, "sms": sms, "sm_mhz": mhz}
 
 
+def in_kernel_clock(probe: dict, launches: int) -> dict:
+    """The clock probe's reading of a region: the mean SM clock over the CTAs' lives (SM
+    cycle counter over the global nanosecond timer) and the CTAs each launch ran."""
+    if not probe or not probe.get("ns"):
+        return {"sm_ghz_in_kernel": None}
+    return {"sm_ghz_in_kernel": probe["cycles"] / probe["ns"],
+            "ctas_per_launch": probe["ctas"] / launches if launches else None,
+            "in_kernel_source": "clock64 / %globaltimer over every CTA of every launch (gemm_read_clock)"}
+
+
+def tensor_peak_at_kernel_clock(tflops: float, clocks: dict, sms: int) -> dict:
+    """The dense-bf16 tensor peak at the clock the kernel ran at, for all SMs and for the
+    SMs its CTAs occupied (one CTA per SM), and the achieved rate's fraction of each."""
+    ghz = (clocks or {}).get("sm_ghz_in_kernel")
+    if not ghz:
+        return None
+    used = (clocks.get("ctas_per_launch") or sms)
+    peak_all = sms * RATED_FLOP_PER_CLK_PER_SM * ghz / 1e3
+    peak_used = used * RATED_FLOP_PER_CLK_PER_SM * ghz / 1e3
+    return {"sm_ghz": ghz, "peak_all_sms": peak_all, "frac_all_sms": tflops / peak_all,
+            "sms_used": used, "peak_sms_used": peak_used, "frac_sms_used": tflops / peak_used,
+            "unit": "TFLOP/s"}
+
+
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     for rel in sources:
@@ -516,7 +540,10 @@ def bench_ours(args, w: Workload):
         opts["mode"] = "unicast"
         if opts.get("cta_group", 1) == 2 and opts.get("cluster_m", 1) > 2 and opts.get("cluster_n", 1) == 1:
             opts["cluster_m"] = 2
-    g = gemm.Gemm(local, layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out, **opts)
+    # The clock probe adds each CTA's SM cycles and nanoseconds to handle-owned counters
+    # (two timer reads and three atomics per CTA), read between the regions below.
+    g = gemm.Gemm(local, layout_a=w.layout_a, layout_b=w.layout_b, layout_c=w.layout_c, out_type=w.out,
+                  clock_probe=1, **opts)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     s, plan = gemm.gemm_plan(g.options, w.M, w.N, w.K, w.batch, sms)
     g.check(s)
@@ -555,6 +582,7 @@ def bench_ours(args, w: Workload):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     launches0 = g.launches
+    g.read_clock(stream)                               # clears the probe: only timed launches count
     barrier(dist)
     torch.cuda.synchronize(device)
     nv = NvmlClocks(device)
@@ -576,6 +604,7 @@ def bench_ours(args, w: Workload):
         torch.cuda.synchronize(device)
         wall1 = time.perf_counter()
         wall = wall1 - wall0
+        kclk = g.read_clock(stream)                    # after the timed region, before the sustained one
         barrier(dist)
         launches = g.launches - launches0
         step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
@@ -585,6 +614,7 @@ def bench_ours(args, w: Workload):
             # about sustain_s, each region between its own events, to see the rate and the
             # clocks under sustained load (power cap) beside the reported burst.
             sustained = sustained_region(g, copies, stream, args.steps, local_s, args.sustain_s, device, w.flops)
+            kclk_sus = g.read_clock(stream)
     g.check(g.query_status(stream))
     elapsed, units = aggregate(dist, local_s, float(w.flops) * args.steps, device)
     value = units / elapsed / 1e12
@@ -608,9 +638,12 @@ def bench_ours(args, w: Workload):
                     "frac": achieved / hbm_peak, "peak_source": f"hbm_gbs (copy) of {peaks_kind}",
                     "algorithmic_bytes_per_launch": w.min_hbm_bytes()}
     clocks = clk.summary(wall0, wall1) if nv.ok else clk.summary()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    clocks.update(in_kernel_clock(kclk, launches))
     if sustained is not None:
         t0, t1, sus = sustained
-        sus["clocks"] = nv.summary(t0, t1) if nv.ok else None
+        sus["clocks"] = nv.summary(t0, t1) if nv.ok else {}
+        sus["clocks"].update(in_kernel_clock(kclk_sus, sus["launches"]))
         if roofline["bound"] == "tensor":
             sus_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
             sus.update({"frac_of_sustained_peak": sus["tflops_median"] / sus_peak, "sustained_peak": sus_peak,
@@ -625,6 +658,10 @@ def bench_ours(args, w: Workload):
         sus_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         roofline.update({"sustained_peak": sus_peak, "frac_of_sustained_peak": achieved / sus_peak})
     if roofline["bound"] == "tensor":
+        roofline["at_kernel_clock"] = tensor_peak_at_kernel_clock(achieved, clocks, sms)
+        if sustained is not None:
+            roofline["sustained"]["at_kernel_clock"] = tensor_peak_at_kernel_clock(
+                roofline["sustained"]["tflops_median"], roofline["sustained"]["clocks"], sms)
         rated = rated_tensor_peak(device, clocks)
         roofline.update({"rated_peak": rated["tflops"], "frac_of_rated": achieved / rated["tflops"],
                          "rated_peak_source": f"{rated['sms']} SMs x {RATED_FLOP_PER_CLK_PER_SM} FLOP/clk x "

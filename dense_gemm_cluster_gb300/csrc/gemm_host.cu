@@ -42,6 +42,8 @@ namespace {
 
 constexpr int kMaxSmemPerCta = 232448;        // 227 KB opt-in shared memory per block on sm_103
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// The clock probe's counters: three per SM slot.
+constexpr size_t kClockBytes = 3 * dgc::CLOCK_PROBE_SLOTS * sizeof(unsigned long long);
 constexpr int64_t kMinSplitBlocks = 16;         // k-blocks per cluster before a sub-wave problem is split wider
 constexpr double kMinTailUs = 4.0;              // saved last-wave time worth a stream-K split
 constexpr double kFlopPerUsPerSm = 1.5e9 / 152; // per-SM tensor rate for that estimate (1.5 PFLOP/s over 152 SMs)
@@ -87,6 +89,8 @@ gemm_status_t resolve(const gemm_options_t& o, int64_t M, int64_t N, int64_t K, 
         return fail(err, GEMM_ERR_INVALID_ARG, "group_m, max_clusters and stages must be >= 0");
     if (o.host_parts < 0 || o.host_parts > kHostChunks)
         return fail(err, GEMM_ERR_INVALID_ARG, "host_parts must be between 0 and %d", kHostChunks);
+    if (o.clock_probe != 0 && o.clock_probe != 1)
+        return fail(err, GEMM_ERR_INVALID_ARG, "clock_probe must be 0 or 1");
     if (o.schedule < 0 || o.schedule > 3)
         return fail(err, GEMM_ERR_INVALID_ARG,
                     "schedule must be 0 (auto), 1 (whole tiles), 2 (stream-K tail) or 3 (cluster launch control)");
@@ -370,10 +374,16 @@ extern "C" gemm_status_t gemm_create(gemm_handle_t* out, const gemm_options_t* o
     h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     e = cudaMalloc(&h->d_status, 16);
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 16);
+    if (e == cudaSuccess && opt->clock_probe) {
+        e = cudaMalloc(&h->d_clock, kClockBytes);
+        if (e == cudaSuccess) e = cudaMemset(h->d_clock, 0, kClockBytes);
+    }
     cudaSetDevice(prev);
     if (e != cudaSuccess) {
+        if (h->d_status) cudaFree(h->d_status);
+        if (h->d_clock) cudaFree(h->d_clock);
         delete h;
-        return fail(nullptr, GEMM_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+        return fail(nullptr, GEMM_ERR_CUDA, "status word / clock counters: %s", cudaGetErrorString(e));
     }
     *out = h;
     return GEMM_OK;
@@ -385,6 +395,7 @@ extern "C" gemm_status_t gemm_destroy(gemm_handle_t h) {
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
     if (h->d_status) cudaFree(h->d_status);
+    if (h->d_clock) cudaFree(h->d_clock);
     if (h->workspace) cudaFree(h->workspace);
     if (h->flags) cudaFree(h->flags);
     for (int i = 0; i < 3; ++i)
@@ -648,6 +659,7 @@ gemm_status_t dgc_host::run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t 
     kp.k_rotate = pl.k_rotate;
     kp.k_serpentine = pl.k_serpentine;
     kp.prefetch_kb = pl.prefetch_kb;
+    kp.clk = h->d_clock;
 
     void* fn = pick_kernel(BN, G, BK);
     const int bi = BN == 256 ? 1 : 0, gi = G - 1, ki = BK == 128 ? 1 : 0;
@@ -782,6 +794,27 @@ extern "C" gemm_status_t gemm_query_status(gemm_handle_t h, void* stream_v) {
     return GEMM_ERR_DEVICE_TIMEOUT;
 }
 
+extern "C" gemm_status_t gemm_read_clock(gemm_handle_t h, void* stream_v, uint64_t out[3]) {
+    if (!h || !out) return fail(h ? &h->err : nullptr, GEMM_ERR_INVALID_ARG, "gemm_read_clock needs a handle and out");
+    if (!h->d_clock) return fail(&h->err, GEMM_ERR_INVALID_ARG, "the handle was created without clock_probe");
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    struct Restore {
+        int d, p;
+        ~Restore() { if (d != p) cudaSetDevice(p); }
+    } restore{h->device, prev};
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_v));
+    unsigned long long c[3 * dgc::CLOCK_PROBE_SLOTS];
+    if (e == cudaSuccess) e = cudaMemcpy(c, h->d_clock, kClockBytes, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->d_clock, 0, kClockBytes);
+    if (e != cudaSuccess) return fail(&h->err, GEMM_ERR_CUDA, "clock counters: %s", cudaGetErrorString(e));
+    out[0] = out[1] = out[2] = 0;
+    for (int sm = 0; sm < dgc::CLOCK_PROBE_SLOTS; ++sm)
+        for (int i = 0; i < 3; ++i) out[i] += c[3 * sm + i];
+    return GEMM_OK;
+}
+
 // ---------------------------------------------------------------------------
 // gemm_run_noalloc: gemm_run without a handle and without any device
 // allocation. The kernel's status record (16 bytes) lives in this file-scope
@@ -855,6 +888,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const gemm_options_t* opt, int device,
     }
     if (opt->schedule == 2)
         return fail(nullptr, GEMM_ERR_UNSUPPORTED, "the stream-K tail needs a workspace; gemm_run_noalloc runs whole tiles");
+    if (opt->clock_probe)
+        return fail(nullptr, GEMM_ERR_UNSUPPORTED, "the clock probe's counters belong to a handle; gemm_run_noalloc has none");
     if (opt->mode == GEMM_MODE_MCAST && (opt->mcast_a || opt->mcast_b) && world_is_multi_gpu())
         return fail(nullptr, GEMM_ERR_UNSUPPORTED,
                     "cluster multicast is single-GPU only; WORLD_SIZE > 1 requires unicast or the pair MMA");

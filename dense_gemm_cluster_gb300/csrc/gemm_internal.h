@@ -29,6 +29,7 @@ struct gemm_handle_s {
     int device = 0;
     int sm_count = 0;
     unsigned int* d_status = nullptr;
+    unsigned long long* d_clock = nullptr;   // clock probe: cycles, nanoseconds, CTAs
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     std::string err;
     // Host-buffer entry points: device staging for A, B and C (grown on demand),

@@ -79,6 +79,7 @@ enum : uint32_t {
 };
 
 constexpr int TILE_RING = 4;   // cluster-launch-control responses in flight per cluster
+constexpr int CLOCK_PROBE_SLOTS = 256;   // per-SM counter slots of the clock probe (%smid modulo this)
 
 struct KernelParams {
     int M, N, K;             // problem (after any transpose for column-major C)
@@ -112,6 +113,7 @@ struct KernelParams {
     int k_rotate;            // 1: whole tiles start their k walk at a tile-dependent k-block
     int k_serpentine;        // 1: a cluster's successive whole tiles alternate their k direction
     int prefetch_kb;         // k-blocks of the first tile prefetched into L2 before waiting for the previous grid
+    unsigned long long* clk; // clock probe: CLOCK_PROBE_SLOTS x (cycles, ns, CTAs), or null
 };
 
 enum : int { L2_HINT_NONE = 0, L2_HINT_EVICT_FIRST = 1, L2_HINT_EVICT_LAST = 2 };
@@ -877,6 +879,16 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (p.prefetch_kb > 0 && (warp == 0 || warp == 6) && lane == 0)
         prefetch_first_stages<G, BK>(p, operand_plan(warp == 0), warp == 0, cx, cy, rx, ry, BN, BN_CTA, cluster,
                                      clusters, p.prefetch_kb);
+    // Clock probe: SM cycles and wall nanoseconds from here to the A producer's last
+    // load, read by that producer thread where the reads cost nothing: before the wait
+    // for the previous grid and after its last load (the clock is the SM's, whatever
+    // runs on it; the adds then overlap the last MMAs and the epilogue).
+    long long probe_c0 = 0;
+    uint64_t probe_t0 = 0;
+    if (p.clk && threadIdx.x == 0) {
+        probe_c0 = clock64();
+        probe_t0 = globaltimer_ns();
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     ClcCtx clc_ctx;
@@ -906,6 +918,13 @@ dgc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 produce<G, BK, WALK_PLAIN>(p, op, is_a, smem_u32(&full_bar[0]), smem_u32(&empty_bar[0]), rank,
                                            leader, cx, cy, rx, ry, BN, BN_CTA, abort_flag, cluster, clusters, S,
                                            &clc_ctx, smem_u32(&ring_empty[0]));
+            if (p.clk && is_a) {
+                // One slot of three counters per SM: no two co-resident CTAs add to the same word.
+                unsigned long long* slot = p.clk + 3 * (smid() % CLOCK_PROBE_SLOTS);
+                atomicAdd(&slot[0], (unsigned long long)(clock64() - probe_c0));
+                atomicAdd(&slot[1], (unsigned long long)(globaltimer_ns() - probe_t0));
+                atomicAdd(&slot[2], 1ull);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer

@@ -43,7 +43,8 @@ class gemm_options_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "mode", "mcast_a", "mcast_b", "cluster_m", "cluster_n", "cta_group", "layout_a", "layout_b",
         "layout_c", "out_type", "block_n", "block_k", "stages", "max_clusters", "group_m", "schedule")] + [
-        ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_int), ("host_parts", ctypes.c_int)]
+        ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_int), ("host_parts", ctypes.c_int),
+        ("clock_probe", ctypes.c_int)]
 
 
 class gemm_plan_t(ctypes.Structure):
@@ -74,6 +75,8 @@ _lib.gemm_run_strided_batched_host.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64,
 _lib.gemm_run_strided_batched_host.restype = _i32
 _lib.gemm_query_status.argtypes = [_vp, _vp]
 _lib.gemm_query_status.restype = _i32
+_lib.gemm_read_clock.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint64)]
+_lib.gemm_read_clock.restype = _i32
 _lib.gemm_plan.argtypes = [_OPT_P, _i64, _i64, _i64, _i64, _i32, ctypes.POINTER(gemm_plan_t)]
 _lib.gemm_plan.restype = _i32
 _lib.gemm_status_string.argtypes = [_i32]
@@ -175,6 +178,14 @@ def gemm_query_status(h, stream=None) -> int:
     return _lib.gemm_query_status(h, _stream(stream))
 
 
+def gemm_read_clock(h, stream=None):
+    """Returns (status, (cycles, nanoseconds, ctas)) of the handle's clock probe since the last
+    read, and clears the counters."""
+    out = (ctypes.c_uint64 * 3)()
+    s = _lib.gemm_read_clock(h, _stream(stream), out)
+    return s, (int(out[0]), int(out[1]), int(out[2]))
+
+
 def gemm_plan(opt: gemm_options_t, M, N, K, batch=1, sm_count=152):
     """Returns (status, gemm_plan_t); sm_count defaults to GB300's 152 SMs."""
     p = gemm_plan_t()
@@ -231,7 +242,7 @@ class Gemm:
     keywords: mode, mcast_a, mcast_b, cluster_m, cluster_n, cta_group (1, 2, or 0 for the pair
     wherever the cluster's extent along M is even), layout_a/b/c ("row" or
     "col"), out_type ("bf16" or "f32"), block_n, block_k, stages, max_clusters, group_m,
-    schedule ("auto", "dp", "stream_k", "clc"), wait_timeout_ns, host_parts).
+    schedule ("auto", "dp", "stream_k", "clc"), wait_timeout_ns, host_parts, clock_probe).
 
     Buffers are torch tensors or integer addresses (numpy arrays for the host entry points);
     sizes, leading dimensions and strides are in elements; `stream` is a torch.cuda.Stream, a
@@ -269,6 +280,14 @@ class Gemm:
         """run_strided_batched() on host buffers, pipelined over the batch."""
         self.check(gemm_run_strided_batched_host(self.handle, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, batch,
                                                  alpha, beta, stream))
+
+    def read_clock(self, stream=None) -> dict:
+        """The clock probe (options clock_probe=1) since the last read: SM cycles, nanoseconds
+        and CTAs summed over the kernel's CTAs, and their ratio, the mean SM clock in GHz.
+        Synchronises `stream` and clears the counters."""
+        s, (c, ns, n) = gemm_read_clock(self.handle, stream)
+        self.check(s)
+        return {"cycles": c, "ns": ns, "ctas": n, "ghz": c / ns if ns else None}
 
     def query_status(self, stream=None) -> int:
         """Synchronises `stream` and returns the status of the runs on it (a bounded in-kernel

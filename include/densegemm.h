@@ -121,6 +121,13 @@ typedef struct {
                            host copies with the GEMMs, 1 to 8 (fewer when the split dimension
                            is short: parts are multiples of 256 lines); 0 = the count a model
                            of the copy and GEMM times picks */
+    int clock_probe;    /* 1: every GEMM launch on this handle adds, per CTA, the SM cycles
+                           (clock64) and the %globaltimer nanoseconds from the end of its
+                           prologue to its last operand load, and one to a CTA count, to device
+                           counters the handle owns, one set per SM (gemm_read_clock sums
+                           them): the clock the kernel actually ran at, under load. Two timer
+                           reads and three uncontended atomics per CTA, where the issuing
+                           thread would wait anyway. 0 = off; gemm_run_noalloc refuses 1. */
 } gemm_options_t;
 
 /* What gemm_run would launch for a given problem (host arithmetic only). */
@@ -235,6 +242,14 @@ gemm_status_t gemm_run_strided_batched_host(gemm_handle_t h, int64_t M, int64_t 
  * receiver's mbarrier waits for bytes another CTA announced; here every such
  * wait is bounded and its expiry is reported instead of hanging). */
 gemm_status_t gemm_query_status(gemm_handle_t h, void *stream);
+
+/* Synchronizes `stream`, copies the handle's clock-probe counters to out[0] (SM
+ * cycles), out[1] (nanoseconds) and out[2] (CTAs counted), summed over the SMs and the launches
+ * since the last read, then clears them; out[0] / out[1] is the mean SM clock in
+ * GHz over the CTAs' lifetimes. GEMM_ERR_INVALID_ARG without a handle or out, or
+ * for a handle created without options.clock_probe; GEMM_ERR_CUDA if a copy fails.
+ * (Measurement plumbing; no page passage.) */
+gemm_status_t gemm_read_clock(gemm_handle_t h, void *stream, uint64_t out[3]);
 
 /* Host-only planning: validates `opt` and the problem as gemm_run would and
  * fills `plan`. Needs no GPU; `sm_count` stands in for the device's SM count. */

@@ -103,6 +103,7 @@ def test_plan_auto_cta_group_pairs_even_cluster_rows(lib):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(cta_group=-1), 2),
+    (dict(clock_probe=2), 1),
     (dict(cta_group=3), 2),
     (dict(cluster_m=3), 2),
     (dict(cluster_m=4, cluster_n=4), 2),
@@ -235,6 +236,7 @@ def test_gemm_entry_points_refuse_a_null_handle_before_any_cuda_call(lib):
     assert lib.gemm_run_strided_batched_host(None, 8, 8, 8, a, 8, 64, a, 8, 64, a, 8, 64, 2, 1.0, 0.0) == \
         lib.GEMM_ERR_INVALID_ARG
     assert lib.gemm_query_status(None) == lib.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_read_clock(None)[0] == lib.GEMM_ERR_INVALID_ARG
     assert lib.gemm_destroy(None) == lib.GEMM_OK
     assert lib.gemm_launch_count(None) == -1
 
@@ -275,6 +277,9 @@ def test_noalloc_checks_options_before_the_device(lib):
     assert run(lib.make_options(schedule="stream_k"), 0, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == \
         lib.GEMM_ERR_UNSUPPORTED
     assert "workspace" in lib.gemm_last_error(None)
+    assert run(lib.make_options(clock_probe=1), 0, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == \
+        lib.GEMM_ERR_UNSUPPORTED
+    assert "clock probe" in lib.gemm_last_error(None)
     assert run(lib.make_options(), 0, -1, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
     assert run(lib.make_options(), 99, 256, 256, 256, a, 256, a, 256, a, 256, 1.0, 0.0) == lib.GEMM_ERR_INVALID_ARG
 

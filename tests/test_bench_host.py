@@ -121,3 +121,15 @@ def test_nvml_clock_summary_windows_and_reasons():
     assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
     c.ok = False
     assert c.summary(0.0, 9.0)["reasons"] == ["nvml unavailable"]
+
+
+def test_in_kernel_clock_and_the_tensor_peak_at_that_clock():
+    import bench
+    c = bench.in_kernel_clock({"cycles": 18_670_000_000, "ns": 10_000_000_000, "ctas": 2880}, 20)
+    assert c["sm_ghz_in_kernel"] == pytest.approx(1.867) and c["ctas_per_launch"] == 144
+    r = bench.tensor_peak_at_kernel_clock(1909.6, c, 152)
+    assert r["peak_all_sms"] == pytest.approx(152 * 8192 * 1.867 / 1e3)
+    assert r["peak_sms_used"] == pytest.approx(144 * 8192 * 1.867 / 1e3)
+    assert r["frac_sms_used"] == pytest.approx(1909.6 / (144 * 8192 * 1.867 / 1e3))
+    assert bench.in_kernel_clock({"cycles": 0, "ns": 0, "ctas": 0}, 20) == {"sm_ghz_in_kernel": None}
+    assert bench.tensor_peak_at_kernel_clock(1000.0, {"sm_ghz_in_kernel": None}, 152) is None
