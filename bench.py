@@ -116,6 +116,21 @@ def in_kernel_clock(probe: dict, launches: int) -> dict:
             "in_kernel_source": "clock64 / %globaltimer over every CTA of every launch (gemm_read_clock)"}
 
 
+SMEM_PORT_BYTES_PER_CLK = 128   # shared-memory bytes an SM moves per clock (reads and writes together)
+
+
+def smem_port_bound(block_m: int, block_n: int, cta_group: int) -> dict:
+    """Shared-memory traffic per tensor clock of one CTA and the tensor utilisation the port
+    allows: per K = 16 step a CTA's MMA reads its A rows (block_m x 16) and its share of B's
+    columns (block_n / cta_group x 16) from shared memory, and TMA has written the same bytes
+    there; the step takes 2 * block_m * block_n * 16 / 8192 tensor clocks."""
+    step_bytes = 2 * 2 * 16 * (block_m + block_n // cta_group)     # (write + read) x bf16 x K16
+    clks = 2 * block_m * block_n * 16 / RATED_FLOP_PER_CLK_PER_SM
+    per_clk = step_bytes / clks
+    return {"bytes_per_tensor_clk": per_clk, "port_bytes_per_clk": SMEM_PORT_BYTES_PER_CLK,
+            "tensor_util_bound": min(1.0, SMEM_PORT_BYTES_PER_CLK / per_clk)}
+
+
 def tensor_peak_at_kernel_clock(tflops: float, clocks: dict, sms: int) -> dict:
     """The dense-bf16 tensor peak at the clock the kernel ran at, for all SMs and for the
     SMs its CTAs occupied (one CTA per SM), and the achieved rate's fraction of each."""
@@ -659,6 +674,8 @@ def bench_ours(args, w: Workload):
         roofline.update({"sustained_peak": sus_peak, "frac_of_sustained_peak": achieved / sus_peak})
     if roofline["bound"] == "tensor":
         roofline["at_kernel_clock"] = tensor_peak_at_kernel_clock(achieved, clocks, sms)
+        if roofline["at_kernel_clock"]:
+            roofline["at_kernel_clock"]["smem_port"] = smem_port_bound(plan.block_m, plan.block_n, plan.cta_group)
         if sustained is not None:
             roofline["sustained"]["at_kernel_clock"] = tensor_peak_at_kernel_clock(
                 roofline["sustained"]["tflops_median"], roofline["sustained"]["clocks"], sms)

@@ -133,3 +133,15 @@ def test_in_kernel_clock_and_the_tensor_peak_at_that_clock():
     assert r["frac_sms_used"] == pytest.approx(1909.6 / (144 * 8192 * 1.867 / 1e3))
     assert bench.in_kernel_clock({"cycles": 0, "ns": 0, "ctas": 0}, 20) == {"sm_ghz_in_kernel": None}
     assert bench.tensor_peak_at_kernel_clock(1000.0, {"sm_ghz_in_kernel": None}, 152) is None
+
+
+def test_smem_port_bound_of_the_tile_shapes():
+    # Per K = 16 step of one CTA: TMA writes and the MMA reads the A rows and the CTA's share of
+    # B's columns; a 128 x 256 single-CTA tile moves 192 B per tensor clock through a 128 B port.
+    import bench
+    one = bench.smem_port_bound(128, 256, 1)
+    assert one["bytes_per_tensor_clk"] == pytest.approx(192.0) and one["tensor_util_bound"] == pytest.approx(2 / 3)
+    pair = bench.smem_port_bound(128, 256, 2)
+    assert pair["bytes_per_tensor_clk"] == pytest.approx(128.0) and pair["tensor_util_bound"] == 1.0
+    narrow = bench.smem_port_bound(128, 128, 1)
+    assert narrow["bytes_per_tensor_clk"] == pytest.approx(256.0) and narrow["tensor_util_bound"] == pytest.approx(0.5)
