@@ -378,13 +378,14 @@ extern "C" gemm_status_t gemm_create(gemm_handle_t* out, const gemm_options_t* o
         e = cudaMalloc(&h->d_clock, kClockBytes);
         if (e == cudaSuccess) e = cudaMemset(h->d_clock, 0, kClockBytes);
     }
-    cudaSetDevice(prev);
     if (e != cudaSuccess) {
-        if (h->d_status) cudaFree(h->d_status);
+        if (h->d_status) cudaFree(h->d_status);   // with the handle's device current
         if (h->d_clock) cudaFree(h->d_clock);
+        cudaSetDevice(prev);
         delete h;
         return fail(nullptr, GEMM_ERR_CUDA, "status word / clock counters: %s", cudaGetErrorString(e));
     }
+    cudaSetDevice(prev);
     *out = h;
     return GEMM_OK;
 }
