@@ -36,7 +36,14 @@
 // Tile order is a static persistent stride over cluster tiles ("Clusters,
 // distributed shared memory & cluster launch control", section "The second
 // wall"), rastered in bands of group_m cluster-rows so that co-running
-// clusters share A and B tiles in L2.
+// clusters share A and B tiles in L2 (with the serpentine walk, odd bands walk
+// their columns from the last). The tiles after the last full wave may be split
+// by k-blocks evenly over all clusters (stream-K: each cluster runs its pieces
+// before its whole tiles; the piece holding a tile's first k-block adds the
+// others' fp32 partials in cluster order, so the sum is deterministic). With
+// cluster launch control every tile is its own cluster launch, and running
+// clusters cancel pending ones and take their tiles (section "Cluster launch
+// control").
 //
 // L2 traffic: when the tile grid is one tile wide, the operand that each tile
 // reads alone is loaded with an evict-first policy and the one every tile reads
@@ -50,6 +57,10 @@
 // Every wait is bounded by wait_timeout_ns of %globaltimer; on expiry the
 // thread records a status word in global memory, raises a CTA-wide abort flag
 // and its role stops, so the kernel always returns.
+//
+// Clock probe (optional): the A producer adds its CTA's SM cycles and
+// %globaltimer nanoseconds, from the end of the prologue to its last load, to
+// its SM's slot of a counter buffer: the clock the kernel ran at.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
