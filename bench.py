@@ -36,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from dense_gemm_cluster_gb300 import inputs, traffic  # noqa: E402
+from dense_gemm_cluster_gb300 import inputs  # noqa: E402
 from dense_gemm_cluster_gb300.workloads import (ATTENTION_WORKLOADS, DEFAULT, WORKLOADS,  # noqa: E402
                                                 AttentionWorkload, Workload)
 
