@@ -41,6 +41,22 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib._lib, n)
 
 
+def test_headers_are_plain_c(tmp_path):
+    # The ABI is C: every header compiles on its own as C99 and C11, pedantically, without CUDA's
+    # headers (streams cross the boundary as void *).
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    headers = sorted(fn for fn in os.listdir(os.path.join(ROOT, "include")) if fn.endswith(".h"))
+    src = tmp_path / "h.c"
+    src.write_text("".join(f'#include "{h}"\n' for h in headers) + "int main(void) { return 0; }\n")
+    for std in ("c99", "c11"):
+        r = subprocess.run([cc, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                            "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(lib):
     assert lib.gemm_status_string(0) == "GEMM_OK"
     assert lib.gemm_status_string(5) == "GEMM_ERR_DEVICE_TIMEOUT"
