@@ -57,6 +57,50 @@ def test_headers_are_plain_c(tmp_path):
         assert r.returncode == 0, r.stderr
 
 
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "densegemm.h"
+int main(void) {
+    gemm_options_t o;
+    gemm_options_default(&o);
+    o.cta_group = 0; o.cluster_m = 4; o.mode = GEMM_MODE_MCAST; o.mcast_b = 1;
+    gemm_plan_t p;
+    gemm_status_t s = gemm_plan(&o, 8192, 8192, 8192, 1, 152, &p);
+    if (s != GEMM_OK) { printf("plan %s\n", gemm_status_string(s)); return 1; }
+    gemm_work_item_t items[64];
+    int64_t n = gemm_schedule_work(p.tiles, 504, 64, 36, 0, items, 64);
+    o.cta_group = 3;
+    gemm_status_t bad = gemm_plan(&o, 8192, 8192, 8192, 1, 152, &p);
+    printf("%d %d %lld %lld %d %d %s\n", p.cta_group, p.group_b, (long long)p.tiles, (long long)n,
+           (int)items[0].kind, (int)bad, gemm_last_error(NULL));
+    return 0;
+}
+"""
+
+
+def test_a_c_program_links_against_the_library_and_plans(lib, tmp_path):
+    # The boundary seen from C: the header, the shared library and the host-only calls, no GPU.
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from dense_gemm_cluster_gb300 import build
+    so_dir = build.BUILD_DIR
+    src, exe = tmp_path / "abi.c", tmp_path / "abi"
+    src.write_text(C_PROGRAM)
+    r = subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-L", so_dir, "-ldensegemm",
+                        f"-Wl,-rpath,{so_dir}", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stdout + out.stderr
+    cta_group, group_b, tiles, n_items, kind0, bad, *msg = out.stdout.split()
+    # Automatic pair on an even cluster extent; 36 clusters walk 512 tiles: the first takes its
+    # stream-K pieces first (kind 1 or 2), then 14 whole tiles.
+    assert (cta_group, group_b, tiles) == ("2", "2", "512")
+    assert int(n_items) == 14 + 1 and kind0 in ("1", "2")
+    assert bad == "2" and "cta_group" in " ".join(msg)
+
+
 def test_status_strings(lib):
     assert lib.gemm_status_string(0) == "GEMM_OK"
     assert lib.gemm_status_string(5) == "GEMM_ERR_DEVICE_TIMEOUT"
